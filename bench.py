@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Throughput of paged chunked-prefill attention on GB300.
+
+One bench step is one pass of the whole hot path over the workload: the
+10,000-token Llama-3-8B-shaped prompt (H_q 32, H_kv 8, d 128, block 128,
+kv_segment_size 1024) processed as 5 chunks of 2048 tokens, each chunk one
+chunked_prefill_attention call (K/V write fused) over the paged cache.
+
+Printed (rank 0, one JSON line): algorithmic attention TFLOP/s =
+4 * H_q * d * visible pairs / time, with the roofline of the attention
+kernel, the end-to-end number through the Python API with host buffers, the
+oracle timed on the host cores, the SM clocks seen during the timed region,
+and a secondary line for the decode-heavy mixed step (KV-read GB/s).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "chunk-attn TFLOP/s (algorithmic, visible pairs only)"
+UNIT = "TFLOP/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [line.split(",") for line in open(self.path).read().strip().splitlines() if line.strip()]
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and "Active" == r[5 + i].strip()})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic_record():
+    """dram bytes per launch of the attention kernel from the committed ncu
+    summary, only if the kernel source has not changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
+    src = os.path.join(ROOT, "chunked_prefill_paged_gb300", "csrc", "attn_tc.cu")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if rec.get("attn_tc_sha256") != h:
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_sample(w: W.Workload, t_cpu, seconds: float):
+    """Time the fp64 oracle on host cores over a bounded sample of the last
+    chunk's rows (the heaviest step).  Returns (TFLOP/s, cores, description)."""
+    import oracle
+    sh = w.shape
+    ob_pool_k = t_cpu["k_cache"]
+    ob_pool_v = t_cpu["v_cache"]
+    # the cache the last chunk reads: the oracle's own writes of the earlier chunks
+    for step in w.steps[:-1]:
+        ob = oracle.Batch(step.cached_seq_len, step.num_new_tokens, w.block_table)
+        rows = step.token_rows
+        ob_pool_k, ob_pool_v = oracle.kv_write(ob, t_cpu["k"][rows], t_cpu["v"][rows], ob_pool_k, ob_pool_v,
+                                               num_heads_kv=sh.num_heads_kv, head_dim=sh.head_dim,
+                                               block_size=sh.block_size)
+    last = w.steps[-1]
+    ob = oracle.Batch(last.cached_seq_len, last.num_new_tokens, w.block_table)
+    rows = last.token_rows
+    q, k, v = t_cpu["q"][rows], t_cpu["k"][rows], t_cpu["v"][rows]
+    cores = oracle.default_threads()
+    C = int(last.cached_seq_len[0])
+
+    def run(n):
+        sel = np.linspace(0, len(rows) - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention(ob, q, k, v, ob_pool_k, ob_pool_v, num_heads_q=sh.num_heads_q,
+                         num_heads_kv=sh.num_heads_kv, head_dim=sh.head_dim, block_size=sh.block_size,
+                         scale=sh.scale, rows=sel, threads=cores)
+        dt = time.perf_counter() - t0
+        flops = sum(W.attention_flops(C + int(i) + 1, sh.num_heads_q, sh.head_dim) for i in sel)
+        return dt, flops
+
+    dt, _ = run(cores)
+    n = int(max(cores, min(len(rows), cores * seconds / max(dt, 1e-3))))
+    dt, flops = run(n)
+    desc = (f"{n} of {len(rows)} query tokens (all {sh.num_heads_q} heads) of the last 2048-token chunk "
+            f"(cached {C}); fp64, {cores} threads, {dt:.1f} s")
+    return flops / dt / 1e12, cores, desc
+
+
+def to_oracle_np(x: torch.Tensor):
+    x = x.contiguous().cpu()
+    return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 else x.numpy()
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args, rank, world, local):
+    import chunked_prefill_paged_gb300 as cpa
+    from chunked_prefill_paged_gb300 import build
+    build.build()
+    cpa.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+
+    w = W.llama3_8b_prompt()
+    sh = w.shape
+    t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
+    params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    batches = [cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev) for s in w.steps]
+    inputs = [t.step_inputs(s) for s in w.steps]
+    outs = [torch.empty((s.total_new_tokens, sh.num_heads_q, sh.head_dim), dtype=torch.bfloat16, device=dev)
+            for s in w.steps]
+    ws_bytes = max(cpa.workspace_size(b, params) for b in batches)
+    ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops_step = sum(w.flops_per_step())
+    launches_per_step = len(w.steps) + sum(
+        1 for b in batches if cpa.workspace_size(b, params) > 0)  # attention (+ merge when split)
+
+    def one_step(evs=None):
+        for i, (b, (q, k, v), o) in enumerate(zip(batches, inputs, outs)):
+            if evs is not None:
+                evs[i][0].record(stream)
+            cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, o, None, ws, stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    torch.cuda.synchronize(dev)
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError("device error during warm-up")
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launch_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in w.steps] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush, outside the timed region
+        step_ev[k][0].record(stream)
+        one_step(launch_ev[k])
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    kernel_ms = sum(a.elapsed_time(b) for row in launch_ev for a, b in row)
+    total_ms = reduce_max(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    achieved = flops_step * args.steps / (kernel_ms / 1e3) / 1e12
+    status = cpa.last_device_error(stream)
+    if status != cpa.SUCCESS:
+        raise RuntimeError(f"device error in the timed region: {cpa.status_string(status)}")
+
+    # end to end through the API with host buffers: H2D of each chunk's
+    # q / k / v from pinned memory, the call, D2H of the output
+    host_in = [tuple(x.cpu().pin_memory() for x in inp) for inp in inputs]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    dev_in = [tuple(torch.empty_like(x) for x in inp) for inp in inputs]
+    h2d = sum(x.numel() * x.element_size() for inp in host_in for x in inp)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+    def e2e_step():
+        for b, hin, din, o, ho in zip(batches, host_in, dev_in, outs, host_out):
+            for d_, h_ in zip(din, hin):
+                d_.copy_(h_, non_blocking=True)
+            cpa.chunked_prefill_attention(b, params, din[0], din[1], din[2], t.k_cache, t.v_cache, o, None, ws,
+                                          stream)
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        e_ev[k][0].record(stream)
+        e2e_step()
+        e_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), world)
+    e2e_value = world * flops_step * args.steps / (e2e_ms / 1e3) / 1e12
+
+    rec = kernel_traffic_record()
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
+                "traffic": rec["bytes_per_launch"] if rec else None,
+                "kernel": "attn_tc_kernel<128>",
+                "algorithmic_flops_per_launch": flops_step / len(w.steps)}
+
+    secondary = None
+    if not args.no_secondary:
+        secondary = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_cpu = {"q": to_oracle_np(t.q), "k": to_oracle_np(t.k), "v": to_oracle_np(t.v),
+                 "k_cache": to_oracle_np(t.k_cache), "v_cache": to_oracle_np(t.v_cache)}
+        v_, cores, desc = oracle_sample(w, t_cpu, args.cpu_seconds)
+        cpu = {"value": v_, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "chunks_per_step": len(w.steps),
+                   "H_q": sh.num_heads_q, "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim,
+                   "block_size": sh.block_size, "kv_segment_size": sh.kv_segment_size,
+                   "flops_per_step": flops_step, "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "secondary": secondary,
+    }
+    return line
+
+
+def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush):
+    """Decode-heavy mixed step (64 decodes + 4 prefill chunks): KV-read GB/s."""
+    import chunked_prefill_paged_gb300 as cpa
+    w = W.mixed_step()
+    sh = w.shape
+    t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
+    s = w.steps[0]
+    params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
+    q, k, v = t.step_inputs(s)
+    out = torch.empty_like(q)
+    n = cpa.workspace_size(b, params)
+    ws = torch.empty(max(n // 4, 4), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
+    byts = w.bytes_per_step()[0]
+    gbs = byts / (ms / 1e3) / 1e9
+    flops = w.flops_per_step()[0]
+    del t
+    return {"workload": w.name, "metric": "mixed-batch algorithmic GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "bytes_per_step": byts, "tflops": round(flops / (ms / 1e3) / 1e12, 2),
+            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands on the host cores, same metric and workload;
+    each step a bounded sample."""
+    if rank != 0:
+        return None
+    w = W.llama3_8b_prompt()
+    t = w.materialize("cpu", sentinel=W.SENTINEL_ZERO)
+    t_cpu = {"q": to_oracle_np(t.q), "k": to_oracle_np(t.k), "v": to_oracle_np(t.v),
+             "k_cache": to_oracle_np(t.k_cache), "v_cache": to_oracle_np(t.v_cache)}
+    per = max(2.0, 60.0 / max(args.steps + args.warmup, 1))
+    vals = []
+    desc = ""
+    cores = 1
+    t0 = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        v_, cores, desc = oracle_sample(w, t_cpu, per)
+        if i >= args.warmup:
+            vals.append(v_)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals) if vals else 0.0
+    sh = w.shape
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "H_q": sh.num_heads_q,
+                   "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim, "block_size": sh.block_size},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

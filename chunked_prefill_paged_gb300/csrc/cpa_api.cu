@@ -1,0 +1,312 @@
+// cpa_api.cu -- the C ABI of libcpa: host-side checks, work planning, tensor
+// maps, and the launches.  Every entry point is declared in include/cpa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/cpa.h"
+#include "cpa_internal.h"
+#include "launch.h"
+
+namespace cpa {
+
+__device__ int g_device_error;  // first error a kernel recorded (0: none)
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultTimeoutCycles = 2000000000LL;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *err = nullptr;  // device address of g_device_error
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+cpa_status device_info(DeviceInfo &out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CPA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CPA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return CPA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return CPA_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return CPA_ERR_CUDA;
+        d.err = static_cast<int *>(p);
+        d.ready = true;
+    }
+    out = d;
+    // the library is built for sm_103a only
+    if (out.cc_major != 10 || out.cc_minor != 3) return CPA_ERR_UNSUPPORTED;
+    return CPA_SUCCESS;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks every argument that the host can see.  Nothing is launched when
+// this fails.
+cpa_status validate(const cpa_batch *b, const cpa_params *p) {
+    if (!b || !p) return CPA_ERR_INVALID_ARG;
+    if (p->dtype != CPA_DTYPE_FP32 && p->dtype != CPA_DTYPE_BF16) return CPA_ERR_INVALID_ARG;
+    if (p->num_heads_q <= 0 || p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv != 0)
+        return CPA_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return CPA_ERR_INVALID_ARG;
+    if (p->block_size != 16 && p->block_size != 32 && p->block_size != 64 && p->block_size != 128)
+        return CPA_ERR_INVALID_ARG;
+    if (p->num_blocks <= 0) return CPA_ERR_INVALID_ARG;
+    const int ks = p->kv_segment_size;
+    if (ks != 0 && ks != 512 && ks != 1024 && ks != 2048 && ks != 4096) return CPA_ERR_INVALID_ARG;
+    if (ks != 0 && ks % p->block_size != 0) return CPA_ERR_INVALID_ARG;
+    if (!isfinite(p->scale)) return CPA_ERR_INVALID_ARG;
+    if (p->timeout_cycles < 0) return CPA_ERR_INVALID_ARG;
+    if (b->num_reqs < 0 || b->total_new_tokens < 0) return CPA_ERR_INVALID_ARG;
+    if (b->num_reqs == 0) return b->total_new_tokens == 0 ? CPA_SUCCESS : CPA_ERR_INVALID_ARG;
+    if (b->max_blocks_per_seq <= 0) return CPA_ERR_INVALID_ARG;
+    if (!b->h_cached_seq_len || !b->h_num_new_tokens) return CPA_ERR_INVALID_ARG;
+    if (!b->cached_seq_len || !b->num_new_tokens || !b->cu_new_tokens || !b->block_table)
+        return CPA_ERR_INVALID_ARG;
+    long long total = 0;
+    const long long cap = (long long)b->max_blocks_per_seq * p->block_size;
+    for (int r = 0; r < b->num_reqs; ++r) {
+        const long long C = b->h_cached_seq_len[r], N = b->h_num_new_tokens[r];
+        if (C < 0 || N < 0 || C + N > cap || C + N > INT32_MAX / 2) return CPA_ERR_INVALID_ARG;
+        total += N;
+    }
+    if (total != b->total_new_tokens) return CPA_ERR_INVALID_ARG;
+    return CPA_SUCCESS;
+}
+
+bool use_tensor_cores(const cpa_params *p) {
+    if (p->dtype != CPA_DTYPE_BF16) return false;
+    if (p->flags & CPA_FLAG_FORCE_SIMT) return false;
+    const int G = p->num_heads_q / p->num_heads_kv;
+    // a query tile is one TMA box of (64, G, 128 / G): G must divide 128
+    return G <= kTcTileM && (kTcTileM % G) == 0;
+}
+
+struct Plan {
+    int tile_m = 0;
+    int split_len = 0;
+    int direct_units = 0;
+    int split_units = 0;
+    int split_reqs = 0;
+    long long ws_floats = 0;
+};
+
+Plan make_plan(const cpa_batch *b, const cpa_params *p) {
+    Plan pl;
+    pl.tile_m = use_tensor_cores(p) ? kTcTileM : kSimtTileM;
+    pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
+    const int G = p->num_heads_q / p->num_heads_kv;
+    for (int r = 0; r < b->num_reqs; ++r) {
+        const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
+                                       p->head_dim, pl.tile_m, pl.split_len);
+        pl.direct_units += w.direct_units;
+        pl.split_units += w.split_units;
+        pl.split_reqs += w.split_units > 0 ? 1 : 0;
+        pl.ws_floats += w.ws_floats;
+    }
+    return pl;
+}
+
+int elem_bytes(const cpa_params *p) { return p->dtype == CPA_DTYPE_FP32 ? 4 : 2; }
+
+cpa_status encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                  const cuuint32_t *box) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CPA_ERR_CUDA;
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CPA_SUCCESS : CPA_ERR_CUDA;
+}
+
+cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, const void *k_new, const void *v_new,
+                        const void *k_cache, const void *v_cache, TcMaps &m) {
+    const cuuint64_t D = (cuuint64_t)p->head_dim, Hq = (cuuint64_t)p->num_heads_q, Hkv = (cuuint64_t)p->num_heads_kv;
+    const cuuint64_t T = (cuuint64_t)b->total_new_tokens, bs = (cuuint64_t)p->block_size;
+    const cuuint32_t G = (cuuint32_t)(p->num_heads_q / p->num_heads_kv);
+    {
+        const cuuint64_t dims[3] = {D, Hq, T};
+        const cuuint64_t strides[2] = {D * 2, Hq * D * 2};
+        const cuuint32_t box[3] = {64, G, (cuuint32_t)kTcTileM / G};
+        if (cpa_status s = encode(&m.q, q, 3, dims, strides, box)) return s;
+    }
+    {
+        const cuuint64_t dims[3] = {D, Hkv, T};
+        const cuuint64_t strides[2] = {D * 2, Hkv * D * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcTileN};
+        if (cpa_status s = encode(&m.k_new, k_new, 3, dims, strides, box)) return s;
+        if (cpa_status s = encode(&m.v_new, v_new, 3, dims, strides, box)) return s;
+    }
+    {
+        const cuuint64_t dims[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
+        const cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
+        const cuuint32_t box[4] = {64, 1, (cuuint32_t)bs, 1};
+        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims, strides, box)) return s;
+        if (cpa_status s = encode(&m.v_pool, v_cache, 4, dims, strides, box)) return s;
+    }
+    return CPA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace cpa
+
+using namespace cpa;
+
+extern "C" {
+
+int32_t cpa_version(void) { return 100; }
+
+const char *cpa_status_string(cpa_status s) {
+    switch (s) {
+        case CPA_SUCCESS: return "success";
+        case CPA_ERR_INVALID_ARG: return "invalid argument";
+        case CPA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case CPA_ERR_CUDA: return "CUDA error";
+        case CPA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case CPA_ERR_BAD_BLOCK_ID: return "block id outside the pool";
+        case CPA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params) {
+    if (validate(batch, params) != CPA_SUCCESS || batch->num_reqs == 0) return 0;
+    const Plan pl = make_plan(batch, params);
+    return (size_t)pl.ws_floats * sizeof(float);
+}
+
+cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, void *stream) {
+    if (cpa_status s = validate(batch, params)) return s;
+    if (batch->total_new_tokens == 0) return CPA_SUCCESS;
+    if (!k_new || !v_new || !k_cache || !v_cache) return CPA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return CPA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (cpa_status s = device_info(dev)) return s;
+    KvWriteArgs a{};
+    a.num_reqs = batch->num_reqs;
+    a.max_blocks = batch->max_blocks_per_seq;
+    a.total_tokens = batch->total_new_tokens;
+    a.cached = batch->cached_seq_len;
+    a.cu = batch->cu_new_tokens;
+    a.bt = batch->block_table;
+    a.hkv = params->num_heads_kv;
+    a.bs = params->block_size;
+    a.num_blocks = params->num_blocks;
+    a.head_bytes = params->head_dim * elem_bytes(params);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.err = dev.err;
+    return launch_kv_write(a, dev.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CPA_SUCCESS : CPA_ERR_CUDA;
+}
+
+cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *params, const void *q,
+                                     const void *k_new, const void *v_new, void *k_cache, void *v_cache, void *out,
+                                     float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    if (cpa_status s = validate(batch, params)) return s;
+    if (batch->total_new_tokens == 0) return CPA_SUCCESS;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !out) return CPA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return CPA_ERR_INVALID_ARG;
+    const Plan pl = make_plan(batch, params);
+    const size_t need = (size_t)pl.ws_floats * sizeof(float);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CPA_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if (cpa_status s = device_info(dev)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    AttnArgs a{};
+    a.num_reqs = batch->num_reqs;
+    a.max_blocks = batch->max_blocks_per_seq;
+    a.total_tokens = batch->total_new_tokens;
+    a.cached = batch->cached_seq_len;
+    a.nnew = batch->num_new_tokens;
+    a.cu = batch->cu_new_tokens;
+    a.bt = batch->block_table;
+    a.hq = params->num_heads_q;
+    a.hkv = params->num_heads_kv;
+    a.G = params->num_heads_q / params->num_heads_kv;
+    a.d = params->head_dim;
+    a.bs = params->block_size;
+    a.num_blocks = params->num_blocks;
+    a.scale_log2 = params->scale * 1.4426950408889634f;
+    a.split_len = pl.split_len;
+    a.tile_m = pl.tile_m;
+    a.num_direct_units = pl.direct_units;
+    a.num_split_units = pl.split_units;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.lse = lse;
+    a.ws = static_cast<float *>(workspace);
+    a.fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) ? 1 : 0;
+    a.write_ctas = pl.direct_units + pl.split_units;
+    a.err = dev.err;
+    a.timeout_cycles = params->timeout_cycles > 0 ? params->timeout_cycles : kDefaultTimeoutCycles;
+    a.test_stall = (params->flags & CPA_FLAG_TEST_STALL) ? 1 : 0;
+
+    cudaError_t e;
+    if (pl.tile_m == kTcTileM) {
+        TcMaps maps;
+        if (cpa_status s = make_tc_maps(batch, params, q, k_new, v_new, k_cache, v_cache, maps)) return s;
+        e = launch_attn_tc(a, maps, st);
+    } else {
+        e = launch_attn_simt(a, params->dtype, st);
+    }
+    if (e != cudaSuccess) return CPA_ERR_CUDA;
+    if (pl.split_reqs > 0) {
+        e = launch_attn_merge(a, params->dtype, pl.split_reqs, st);
+        if (e != cudaSuccess) return CPA_ERR_CUDA;
+    }
+    return CPA_SUCCESS;
+}
+
+cpa_status cpa_last_device_error(void *stream) {
+    DeviceInfo dev;
+    if (cpa_status s = device_info(dev)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, dev.err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return CPA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CPA_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemsetAsync(dev.err, 0, sizeof(int), st) != cudaSuccess) return CPA_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return CPA_ERR_CUDA;
+    }
+    return static_cast<cpa_status>(v);
+}
+
+}  // extern "C"

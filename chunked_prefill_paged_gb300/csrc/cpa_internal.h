@@ -1,0 +1,115 @@
+// cpa_internal.h -- definitions shared by the host planner and the kernels
+// of libcpa (not part of the public ABI).
+//
+// Work decomposition.  The active rows of a request are its N_r tokens times
+// the G = H_q / H_kv query heads that share one key/value head ("Prefill
+// Optimisation", section 6, grouped-query attention); they are packed
+// token-major, head-minor, so one tile of rows reads one stream of K/V.  A
+// work unit is (request, kv head, query tile, key range):
+//   * direct units: a query tile with all keys it can see, walked in order
+//     with the running (max, sum, output) carried along;
+//   * split units: requests whose rows fit one tile (decodes, tiny chunks)
+//     are cut into pieces of split_len keys -- the kv_segment_size segments
+//     of "Prefill Processing" (Kernel Interface, Partial KV Segment
+//     Handling) -- each written as a partial (unnormalised output, max,
+//     sum) and merged by attn_merge.
+// Direct units are numbered first (heaviest query tile of each request
+// first), then split units.  Host and device both use request_work() so the
+// launch size and the device-side decode agree.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define CPA_HD __host__ __device__ __forceinline__
+#else
+#define CPA_HD inline
+#endif
+
+namespace cpa {
+
+constexpr int kTcTileM = 128;    // packed query rows per tensor-core tile
+constexpr int kTcTileN = 128;    // keys per K/V tile
+constexpr int kSimtTileM = 16;   // packed query rows per CUDA-core tile
+constexpr int kDefaultSplit = 1024;
+
+// device error codes (match cpa_status)
+constexpr int kErrTimeout = 4;
+constexpr int kErrBadBlock = 5;
+
+CPA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct ReqWork {
+    int direct_units;    // H_kv * query tiles, or 0
+    int split_units;     // H_kv * pieces, or 0
+    int pieces;          // key pieces of a split request (0 when direct)
+    long long ws_floats; // floats of partials for a split request
+};
+
+CPA_HD ReqWork request_work(int C, int N, int G, int hkv, int d, int tile_m, int split_len) {
+    ReqWork w{0, 0, 0, 0};
+    if (N <= 0) return w;
+    const int rows = N * G;
+    const int n_qt = cdiv(rows, tile_m);
+    if (split_len > 0 && n_qt == 1) {
+        const int pieces = cdiv(C + N, split_len);
+        if (pieces > 1) {
+            w.split_units = hkv * pieces;
+            w.pieces = pieces;
+            w.ws_floats = (long long)w.split_units * rows * (d + 2);
+            return w;
+        }
+    }
+    w.direct_units = hkv * n_qt;
+    return w;
+}
+
+// Arguments of every attention kernel (passed by value).
+struct AttnArgs {
+    // batch
+    int num_reqs;
+    int max_blocks;
+    int total_tokens;
+    const int32_t *cached;
+    const int32_t *nnew;
+    const int32_t *cu;
+    const int32_t *bt;
+    // shape
+    int hq, hkv, G, d, bs, num_blocks;
+    float scale_log2;  // softmax scale * log2(e)
+    int split_len;     // 0: no split units
+    int tile_m;
+    int num_direct_units;
+    int num_split_units;
+    // data
+    const void *q;
+    const void *k_new;
+    const void *v_new;
+    void *k_cache;
+    void *v_cache;
+    void *out;
+    float *lse;
+    float *ws;          // partials of split units
+    int fuse_write;     // write new K/V into the pool in the prologue
+    int write_ctas;     // CTAs that share the fused write
+    int *err;           // device error word (first error wins)
+    long long timeout_cycles;
+    int test_stall;     // testing only: withhold the first K tile's copies
+};
+
+// Arguments of the standalone KV write.
+struct KvWriteArgs {
+    int num_reqs, max_blocks, total_tokens;
+    const int32_t *cached;
+    const int32_t *cu;
+    const int32_t *bt;
+    int hkv, bs, num_blocks;
+    int head_bytes;  // d * element bytes: one head's row
+    const void *k_new;
+    const void *v_new;
+    void *k_cache;
+    void *v_cache;
+    int *err;
+};
+
+}  // namespace cpa

@@ -1,0 +1,176 @@
+// device_common.cuh -- device helpers shared by the kernels: work-unit
+// decoding, the paged-slot lookup of an active token, the fused/standalone
+// K/V scatter, and error recording.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "cpa_internal.h"
+
+namespace cpa {
+
+__device__ __forceinline__ void record_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Request owning packed token t: the last r with cu[r] <= t (requests with no
+// tokens are skipped because cu[r] == cu[r + 1]).
+__device__ __forceinline__ int request_of_token(const int32_t *cu, int num_reqs, int t) {
+    int lo = 0, hi = num_reqs;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(cu + mid) <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// A decoded work unit (see cpa_internal.h).
+struct Unit {
+    int r, g, qt, piece;  // piece < 0: direct unit
+    int C, N, cu0;
+    int row0, rows;       // packed rows [row0, row0 + rows) of the request
+    int k_begin, k_end;   // keys [k_begin, k_end) of this unit
+    long long ws_off;     // float offset of the unit's partial (split units)
+};
+
+// Decode unit index `unit`; every lane of the calling warp must take part and
+// gets the same result.  Returns false for an index past the last unit.
+__device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u) {
+    const int lane = threadIdx.x & 31;
+    const bool split = unit >= a.num_direct_units;
+    const int target = split ? unit - a.num_direct_units : unit;
+    int base = 0;
+    long long base_ws = 0;
+    for (int r0 = 0; r0 < a.num_reqs; r0 += 32) {
+        const int r = r0 + lane;
+        ReqWork w{0, 0, 0, 0};
+        if (r < a.num_reqs) w = request_work(__ldg(a.cached + r), __ldg(a.nnew + r), a.G, a.hkv, a.d, a.tile_m,
+                                             a.split_len);
+        const int cnt = split ? w.split_units : w.direct_units;
+        const long long wsf = split ? w.ws_floats : 0;
+        int inc = cnt;
+        long long incw = wsf;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, inc, o);
+            long long tw = __shfl_up_sync(0xffffffffu, incw, o);
+            if (lane >= o) {
+                inc += t;
+                incw += tw;
+            }
+        }
+        const bool hit = cnt > 0 && target >= base + inc - cnt && target < base + inc;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const int rr = r0 + src;
+            const int first = __shfl_sync(0xffffffffu, base + inc - cnt, src);
+            const long long wsb = __shfl_sync(0xffffffffu, base_ws + incw - wsf, src);
+            const int local = target - first;
+            u.r = rr;
+            u.C = __ldg(a.cached + rr);
+            u.N = __ldg(a.nnew + rr);
+            u.cu0 = __ldg(a.cu + rr);
+            u.g = local % a.hkv;
+            const int rows_total = u.N * a.G;
+            if (!split) {
+                const int n_qt = cdiv(rows_total, a.tile_m);
+                u.qt = n_qt - 1 - local / a.hkv;  // heaviest tile of the request first
+                u.piece = -1;
+                u.row0 = u.qt * a.tile_m;
+                u.rows = min(a.tile_m, rows_total - u.row0);
+                const int last_tok = (u.row0 + u.rows - 1) / a.G;
+                u.k_begin = 0;
+                u.k_end = u.C + last_tok + 1;
+                u.ws_off = 0;
+            } else {
+                u.qt = 0;
+                u.piece = local / a.hkv;
+                u.row0 = 0;
+                u.rows = rows_total;
+                u.k_begin = u.piece * a.split_len;
+                u.k_end = min(u.k_begin + a.split_len, u.C + u.N);
+                u.ws_off = wsb + (long long)local * rows_total * (a.d + 2);
+            }
+            return true;
+        }
+        base += __shfl_sync(0xffffffffu, inc, 31);
+        base_ws += __shfl_sync(0xffffffffu, incw, 31);
+    }
+    return false;
+}
+
+// Physical pool row (slot) of absolute position `pos` of request r, or -1
+// when the block id is outside [0, num_blocks) (recorded in *err).
+__device__ __forceinline__ long long slot_of(const int32_t *bt, int max_blocks, int bs, int num_blocks, int r,
+                                             int pos, int *err) {
+    const int blk = __ldg(bt + (long long)r * max_blocks + pos / bs);
+    if (blk < 0 || blk >= num_blocks) {
+        record_error(err, kErrBadBlock);
+        return -1;
+    }
+    return (long long)blk * bs + pos % bs;
+}
+
+// Scatter 16-byte pieces [begin, end) of the new K/V rows into the pool.
+// Piece index = ((t * hkv + g) * pieces_per_head + p): consecutive threads
+// copy consecutive 16 bytes of one token's row, so loads and stores are
+// coalesced.  Active token t of request r lands on the slot of position
+// cached[r] + (t - cu[r]).
+__device__ __forceinline__ void scatter_new_kv(const int32_t *cached, const int32_t *cu, const int32_t *bt,
+                                               int num_reqs, int max_blocks, int hkv, int bs, int num_blocks,
+                                               int head_bytes, const void *k_new, const void *v_new,
+                                               void *k_cache, void *v_cache, long long begin, long long end,
+                                               int stride_start, int stride, int *err) {
+    const int pieces_per_head = head_bytes >> 4;
+    const long long per_token = (long long)hkv * pieces_per_head;
+    for (long long i = begin + stride_start; i < end; i += stride) {
+        const int t = (int)(i / per_token);
+        const int rem = (int)(i - (long long)t * per_token);
+        const int g = rem / pieces_per_head;
+        const int p = rem - g * pieces_per_head;
+        const int r = request_of_token(cu, num_reqs, t);
+        const int pos = __ldg(cached + r) + (t - __ldg(cu + r));
+        const long long slot = slot_of(bt, max_blocks, bs, num_blocks, r, pos, err);
+        if (slot < 0) continue;
+        const long long src = ((long long)t * hkv + g) * head_bytes + p * 16;
+        const long long dst = (slot * hkv + g) * head_bytes + p * 16;
+        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + src));
+        const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(v_new) + src));
+        *reinterpret_cast<uint4 *>(static_cast<char *>(k_cache) + dst) = kv;
+        *reinterpret_cast<uint4 *>(static_cast<char *>(v_cache) + dst) = vv;
+    }
+}
+
+// Share of the fused K/V write done by CTA `cta` of `ctas` (called by
+// `nthreads` threads of the CTA, thread index `tid`).
+__device__ __forceinline__ void fused_write_share(const AttnArgs &a, int cta, int ctas, int tid, int nthreads,
+                                                  int elem_bytes) {
+    const int head_bytes = a.d * elem_bytes;
+    const long long total = (long long)a.total_tokens * a.hkv * (head_bytes >> 4);
+    const long long per = (total + ctas - 1) / ctas;
+    const long long b = (long long)cta * per;
+    const long long e = b + per < total ? b + per : total;
+    if (b >= e) return;
+    scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, head_bytes,
+                   a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, nthreads, a.err);
+}
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ float from_float<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+}  // namespace cpa

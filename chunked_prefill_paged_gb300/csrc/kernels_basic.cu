@@ -1,0 +1,286 @@
+// kernels_basic.cu -- the standalone paged K/V write, the CUDA-core
+// attention kernel (FP32 path, and a BF16 cross-check), and the merge of
+// split-KV partials.
+//
+// Attention semantics ("Prefill Processing", Key Concepts and Kernel
+// Interface; "Prefill Optimisation", section 2): packed row (token t, query
+// head h) of request r sees keys j <= cached_seq_len[r] + (t - cu[r]); keys
+// below cached_seq_len come from the pool through the block table, the rest
+// from the request's new K/V rows.  The running maximum / sum / output are
+// carried across key tiles (online softmax), in the log2 domain: scores are
+// multiplied by scale * log2(e) and exponentiated with exp2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace cpa {
+
+// ------------------------------------------------------------------ KV write
+__global__ void __launch_bounds__(256) kv_write_kernel(KvWriteArgs a) {
+    const long long total = (long long)a.total_tokens * a.hkv * (a.head_bytes >> 4);
+    const int stride = gridDim.x * blockDim.x;
+    scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, a.head_bytes,
+                   a.k_new, a.v_new, a.k_cache, a.v_cache, 0, total, blockIdx.x * blockDim.x + threadIdx.x,
+                   stride, a.err);
+}
+
+cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stream) {
+    const long long total = (long long)a.total_tokens * a.hkv * (a.head_bytes >> 4);
+    if (total == 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    kv_write_kernel<<<(int)blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------- CUDA-core attention
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
+    constexpr int KT = 32;        // keys per shared-memory tile
+    constexpr int RPW = 4;        // rows per warp (4 warps x 4 = kSimtTileM)
+    constexpr int DPL = D / 32;   // output elements per lane
+    static_assert(RPW * 4 == kSimtTileM, "tile rows");
+    __shared__ float q_s[kSimtTileM][D];
+    __shared__ float k_s[KT][D + 1];
+    __shared__ float v_s[KT][D];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (a.fuse_write) fused_write_share(a, blockIdx.x, gridDim.x, tid, 128, (int)sizeof(T));
+
+    Unit u;
+    if (!decode_unit(a, blockIdx.x, u)) return;
+    const T *q = static_cast<const T *>(a.q);
+    const T *k_new = static_cast<const T *>(a.k_new);
+    const T *v_new = static_cast<const T *>(a.v_new);
+    const T *k_pool = static_cast<const T *>(a.k_cache);
+    const T *v_pool = static_cast<const T *>(a.v_cache);
+    const int G = a.G;
+
+    for (int idx = tid; idx < kSimtTileM * D; idx += 128) {
+        const int lr = idx / D, c = idx % D;
+        float x = 0.f;
+        if (lr < u.rows) {
+            const int pr = u.row0 + lr;
+            const int t = u.cu0 + pr / G, h = u.g * G + pr % G;
+            x = to_float(q[((long long)t * a.hq + h) * D + c]) * a.scale_log2;
+        }
+        q_s[lr][c] = x;
+    }
+
+    float m[RPW], l[RPW], o[RPW][DPL];
+    int pos[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[i][c] = 0.f;
+        const int lr = warp * RPW + i;
+        pos[i] = (lr < u.rows) ? u.C + (u.row0 + lr) / G : -1;
+    }
+
+    for (int kb = u.k_begin; kb < u.k_end; kb += KT) {
+        __syncthreads();
+        for (int idx = tid; idx < KT * D; idx += 128) {
+            const int kk = idx / D, c = idx % D;
+            const int j = kb + kk;
+            float kx = 0.f, vx = 0.f;
+            if (j < u.k_end) {
+                if (j < u.C) {
+                    const long long slot = slot_of(a.bt, a.max_blocks, a.bs, a.num_blocks, u.r, j, a.err);
+                    if (slot >= 0) {
+                        const long long e = (slot * a.hkv + u.g) * D + c;
+                        kx = to_float(k_pool[e]);
+                        vx = to_float(v_pool[e]);
+                    }
+                } else {
+                    const long long e = ((long long)(u.cu0 + j - u.C) * a.hkv + u.g) * D + c;
+                    kx = to_float(k_new[e]);
+                    vx = to_float(v_new[e]);
+                }
+            }
+            k_s[kk][c] = kx;
+            v_s[kk][c] = vx;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int lr = warp * RPW + i;
+            if (lr >= u.rows) continue;  // uniform across the warp
+            const int j = kb + lane;
+            float s = -INFINITY;
+            if (j < u.k_end && j <= pos[i]) {
+                float acc = 0.f;
+#pragma unroll 16
+                for (int c = 0; c < D; ++c) acc = fmaf(q_s[lr][c], k_s[lane][c], acc);
+                s = acc;
+            }
+            const float mn = fmaxf(m[i], warp_max(s));
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            const float p = exp2f(s - mu);
+            const float alpha = exp2f(m[i] - mu);
+            l[i] = l[i] * alpha + warp_sum(p);
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) o[i][c] *= alpha;
+#pragma unroll 8
+            for (int jj = 0; jj < KT; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) o[i][c] = fmaf(pj, v_s[jj][lane + 32 * c], o[i][c]);
+            }
+            m[i] = mn;
+        }
+    }
+
+    T *out = static_cast<T *>(a.out);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int lr = warp * RPW + i;
+        if (lr >= u.rows) continue;
+        if (u.piece >= 0) {
+            float *ws = a.ws + u.ws_off;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) ws[(long long)lr * D + lane + 32 * c] = o[i][c];
+            if (lane == 0) {
+                ws[(long long)u.rows * D + lr] = m[i];
+                ws[(long long)u.rows * D + u.rows + lr] = l[i];
+            }
+        } else {
+            const int pr = u.row0 + lr;
+            const int t = u.cu0 + pr / G, h = u.g * G + pr % G;
+            const float inv = 1.f / l[i];
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) out[((long long)t * a.hq + h) * D + lane + 32 * c] = from_float<T>(o[i][c] * inv);
+            if (a.lse && lane == 0) a.lse[(long long)t * a.hq + h] = (m[i] + log2f(l[i])) * 0.69314718055994531f;
+        }
+    }
+}
+
+cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t stream) {
+    const int grid = a.num_direct_units + a.num_split_units;
+    if (grid == 0) return cudaSuccess;
+    if (dtype == CPA_DTYPE_FP32) {
+        if (a.d == 64)
+            attn_simt_kernel<float, 64><<<grid, 128, 0, stream>>>(a);
+        else
+            attn_simt_kernel<float, 128><<<grid, 128, 0, stream>>>(a);
+    } else {
+        if (a.d == 64)
+            attn_simt_kernel<__nv_bfloat16, 64><<<grid, 128, 0, stream>>>(a);
+        else
+            attn_simt_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ split merge
+// Combine the partials of the pieces of one split request for one kv head:
+// M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L,
+// lse = (M + log2 L) ln 2.  Pieces that saw no key (l_s = 0) are skipped.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+    constexpr int DPL = D / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sr = blockIdx.x / a.hkv;  // index among split requests
+    const int g = blockIdx.x % a.hkv;
+    // find the sr-th split request and its workspace base
+    int r = -1, pieces = 0;
+    long long wsb = 0;
+    {
+        int base = 0;
+        long long base_ws = 0;
+        for (int r0 = 0; r0 < a.num_reqs && r < 0; r0 += 32) {
+            const int rr = r0 + lane;
+            ReqWork w{0, 0, 0, 0};
+            if (rr < a.num_reqs) w = request_work(__ldg(a.cached + rr), __ldg(a.nnew + rr), a.G, a.hkv, a.d,
+                                                  a.tile_m, a.split_len);
+            const int cnt = w.split_units > 0 ? 1 : 0;
+            int inc = cnt;
+            long long incw = w.ws_floats;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int t = __shfl_up_sync(0xffffffffu, inc, o);
+                long long tw = __shfl_up_sync(0xffffffffu, incw, o);
+                if (lane >= o) {
+                    inc += t;
+                    incw += tw;
+                }
+            }
+            const bool hit = cnt > 0 && sr == base + inc - 1;
+            const unsigned m = __ballot_sync(0xffffffffu, hit);
+            if (m) {
+                const int src = __ffs(m) - 1;
+                r = r0 + src;
+                wsb = __shfl_sync(0xffffffffu, base_ws + incw - w.ws_floats, src);
+                pieces = __shfl_sync(0xffffffffu, w.pieces, src);
+            }
+            base += __shfl_sync(0xffffffffu, inc, 31);
+            base_ws += __shfl_sync(0xffffffffu, incw, 31);
+        }
+    }
+    if (r < 0) return;
+    const int N = __ldg(a.nnew + r), cu0 = __ldg(a.cu + r);
+    const int rows = N * a.G;
+    const long long unit_floats = (long long)rows * (D + 2);
+    T *out = static_cast<T *>(a.out);
+    for (int lr = warp; lr < rows; lr += 4) {
+        float M = -INFINITY;
+        for (int s = 0; s < pieces; ++s) {
+            const float *p = a.ws + wsb + (long long)(s * a.hkv + g) * unit_floats;
+            const float ls = p[(long long)rows * D + rows + lr];
+            if (ls > 0.f) M = fmaxf(M, p[(long long)rows * D + lr]);
+        }
+        float L = 0.f, o[DPL];
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[c] = 0.f;
+        for (int s = 0; s < pieces; ++s) {
+            const float *p = a.ws + wsb + (long long)(s * a.hkv + g) * unit_floats;
+            const float ls = p[(long long)rows * D + rows + lr];
+            if (!(ls > 0.f)) continue;
+            const float w = exp2f(p[(long long)rows * D + lr] - M);
+            L += ls * w;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) o[c] = fmaf(w, p[(long long)lr * D + lane + 32 * c], o[c]);
+        }
+        const int t = cu0 + lr / a.G, h = g * a.G + lr % a.G;
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) out[((long long)t * a.hq + h) * D + lane + 32 * c] = from_float<T>(o[c] * inv);
+        if (a.lse && lane == 0) a.lse[(long long)t * a.hq + h] = (M + log2f(L)) * 0.69314718055994531f;
+    }
+}
+
+cudaError_t launch_attn_merge(const AttnArgs &a, int dtype, int num_split_reqs, cudaStream_t stream) {
+    const int grid = num_split_reqs * a.hkv;
+    if (grid == 0) return cudaSuccess;
+    if (dtype == CPA_DTYPE_FP32) {
+        if (a.d == 64)
+            attn_merge_kernel<float, 64><<<grid, 128, 0, stream>>>(a);
+        else
+            attn_merge_kernel<float, 128><<<grid, 128, 0, stream>>>(a);
+    } else {
+        if (a.d == 64)
+            attn_merge_kernel<__nv_bfloat16, 64><<<grid, 128, 0, stream>>>(a);
+        else
+            attn_merge_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace cpa

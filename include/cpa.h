@@ -1,0 +1,174 @@
+/*
+ * cpa.h -- C ABI of the GB300 (sm_103a) paged chunked-prefill attention
+ * library (libcpa.so).
+ *
+ * One step of an LLM serving engine hands the library a mixed batch of
+ * active tokens: prefill chunks scheduled under a per-step token budget and
+ * single-token decodes.  Request r has num_new_tokens[r] active tokens whose
+ * queries attend to cached_seq_len[r] tokens of prior K/V -- held in a
+ * block-paged pool and reached through row r of a block table -- and,
+ * causally, to the request's own active tokens.  Active token i of request
+ * r sits at absolute position cached_seq_len[r] + i.  Its new K/V row is
+ * written into the pool slot of that position.
+ *
+ * Sources (page title, section):
+ *   "Prefill Processing" (AWS Neuron vLLM design doc): Key Concepts
+ *     (active tokens, cached KV segments, kv_segment_size, cached_seq_len),
+ *     Kernel Interface (prior_tokens per request, segment count derived
+ *     inside the kernel), Partial KV Segment Handling, Attention Metadata
+ *     (block table, slot mapping, block size, max blocks per sequence),
+ *     Block Allocation (block table rows, unallocated columns).
+ *   "Prefill Optimisation": section 2 (causal equivalence: chunked prefill
+ *     equals one-shot causal attention; online-softmax rescaling across
+ *     tiles), section 6 (grouped-query attention: H_kv key/value heads for
+ *     H_q query heads).
+ *   "Chunked Prefill" (blog note): the greedy decode-first token budget and
+ *     the absolute position offset of each chunk.
+ *
+ * Conventions shared by every entry point:
+ *   - Element type: CPA_DTYPE_BF16 or CPA_DTYPE_FP32; q, k_new, v_new, the
+ *     pools and out share it.
+ *   - q     [T, H_q, d]   contiguous, rows packed by request (cu_new_tokens).
+ *   - k_new [T, H_kv, d]  contiguous; v_new likewise.
+ *   - out   [T, H_q, d]   contiguous.
+ *   - lse   [T, H_q]      float32, natural log of the softmax denominator of
+ *                         the scaled scores (nullable).
+ *   - k_cache, v_cache [num_blocks, block_size, H_kv, d] contiguous: the
+ *     slot of position p of request r is
+ *       block_table[r * max_blocks_per_seq + p / block_size] * block_size
+ *       + p % block_size,
+ *     and a slot is one row of the pool.
+ *   - Query head h reads key/value head h / (H_q / H_kv).
+ *   - Device pointers must be 16-byte aligned.
+ *   - Ownership: the caller allocates and frees every buffer, the workspace
+ *     included.  The library never allocates, frees or synchronises; all
+ *     work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream) and is asynchronous.
+ *   - Errors: return codes, never exceptions or aborts.  Every argument is
+ *     checked on the host before anything is launched; a failed check
+ *     launches nothing.  Block ids read on the device are range-checked:
+ *     an id outside [0, num_blocks) is skipped and recorded, and
+ *     cpa_last_device_error reports it.
+ *   - The caller guarantees that no two active tokens share a slot and that
+ *     no active token's slot lies inside another request's cached range
+ *     (shared prefix blocks are read-only).
+ */
+#ifndef CPA_H_
+#define CPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CPA_SUCCESS = 0,
+    CPA_ERR_INVALID_ARG = 1,     /* a host-side check failed; nothing launched */
+    CPA_ERR_UNSUPPORTED = 2,     /* valid, but not built for this dtype / shape / device */
+    CPA_ERR_CUDA = 3,            /* a CUDA call or launch failed */
+    CPA_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait ran out (kernel returned early) */
+    CPA_ERR_BAD_BLOCK_ID = 5,    /* a block-table entry outside [0, num_blocks) was read */
+    CPA_ERR_WORKSPACE = 6        /* workspace missing or smaller than the size query returned */
+} cpa_status;
+
+typedef enum { CPA_DTYPE_FP32 = 0, CPA_DTYPE_BF16 = 1 } cpa_dtype;
+
+/* flags (cpa_params.flags) */
+#define CPA_FLAG_FUSE_KV_WRITE 0x1u /* attention also writes the new K/V into the pool
+                                       (the write of paged_kv_write, done in the
+                                       attention kernel's prologue) */
+#define CPA_FLAG_FORCE_SIMT 0x2u    /* BF16 only: use the CUDA-core kernel instead of the
+                                       tensor-core kernel (cross-checking) */
+#define CPA_FLAG_NO_SPLIT 0x4u      /* never split one query tile's keys across CTAs */
+#define CPA_FLAG_TEST_STALL 0x100u  /* testing only: the tensor-core kernel withholds the
+                                       copies of one K tile, so its consumers' bounded waits
+                                       expire and the launch reports CPA_ERR_DEVICE_TIMEOUT
+                                       (use with a small timeout_cycles) */
+
+/* Varlen batch descriptor of one step ("Prefill Processing", Scheduler
+ * Output and Attention Metadata).  Device arrays are read by the kernels;
+ * the host mirrors are read by the host for checks and launch sizing and
+ * must hold the same values as the device arrays. */
+typedef struct {
+    int32_t num_reqs;               /* requests in the step (>= 0) */
+    int32_t max_blocks_per_seq;     /* columns of the block table (>= 1 when num_reqs > 0) */
+    int32_t total_new_tokens;       /* T = sum of num_new_tokens */
+    const int32_t *cached_seq_len;  /* device [num_reqs]: prior tokens in the pool (C_r) */
+    const int32_t *num_new_tokens;  /* device [num_reqs]: active tokens (N_r >= 0) */
+    const int32_t *cu_new_tokens;   /* device [num_reqs + 1]: prefix sums of N_r, cu[0] = 0 */
+    const int32_t *block_table;     /* device [num_reqs, max_blocks_per_seq], row-major */
+    const int32_t *h_cached_seq_len;/* host mirror of cached_seq_len */
+    const int32_t *h_num_new_tokens;/* host mirror of num_new_tokens */
+} cpa_batch;
+
+/* Shape and options of one attention layer. */
+typedef struct {
+    int32_t num_heads_q;      /* H_q, a multiple of num_heads_kv */
+    int32_t num_heads_kv;     /* H_kv */
+    int32_t head_dim;         /* d: 64 or 128 */
+    int32_t block_size;       /* tokens per cache block: 16, 32, 64 or 128 */
+    int32_t num_blocks;       /* blocks in each pool */
+    int32_t kv_segment_size;  /* 0 (library chooses) or 512, 1024, 2048, 4096; a multiple of
+                                 block_size ("Prefill Processing", Kernel Interface).  It is the
+                                 unit in which the keys of single-tile requests (decodes) are
+                                 split across CTAs and merged. */
+    float scale;              /* softmax scale applied to q.k (usually 1/sqrt(d)) */
+    int32_t dtype;            /* cpa_dtype */
+    uint32_t flags;           /* CPA_FLAG_* */
+    int64_t timeout_cycles;   /* bound of every device-side wait, in SM clock cycles;
+                                 0 = library default (2e9, about one second) */
+} cpa_params;
+
+/* Bytes of device workspace chunked_prefill_attention needs for this batch
+ * (0 when no request is split).  Reads only host mirrors.  Returns 0 also
+ * when the arguments are invalid; chunked_prefill_attention then reports
+ * the error. */
+size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params);
+
+/* Write the K/V rows of every active token into their pool slots: token i of
+ * request r goes to the slot of position cached_seq_len[r] + i
+ * ("Prefill Processing", Key Concepts: active tokens write new KV to cache;
+ * Attention Metadata: slot_mapping).  A byte-exact copy.  k_new/v_new are
+ * read, k_cache/v_cache written in place.  Only the slots of active tokens
+ * change. */
+cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, const void *k_new,
+                          const void *v_new, void *k_cache, void *v_cache, void *stream);
+
+/* Attention of every active token over its request's cached K/V and,
+ * causally, the request's active tokens ("Prefill Processing", How
+ * Segmentation Works with KV Segments and Kernel Interface; "Prefill
+ * Optimisation", section 2).  For token i of request r, query head h:
+ *   out = sum_j softmax_j(scale * q . k_j) v_j over positions j <= C_r + i,
+ * keys j < C_r read from the pool through the block table, keys j >= C_r
+ * from k_new / v_new.  The cached keys are walked in kv_segment_size pieces
+ * combined by online-softmax merging; the result is the same up to
+ * rounding.  With CPA_FLAG_FUSE_KV_WRITE the new K/V rows are also written
+ * into the pool (as paged_kv_write) in the same launch; without it the pools
+ * are only read.
+ * workspace: device memory of at least chunked_prefill_workspace_size()
+ * bytes (may be NULL when that size is 0); its contents need not be
+ * initialised and are overwritten.  lse may be NULL. */
+cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *params, const void *q,
+                                     const void *k_new, const void *v_new, void *k_cache,
+                                     void *v_cache, void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* Wait for `stream`, then return and clear the first error recorded by a
+ * kernel on the current device since the last call (CPA_SUCCESS if none):
+ * CPA_ERR_DEVICE_TIMEOUT or CPA_ERR_BAD_BLOCK_ID.  CPA_ERR_CUDA if the
+ * stream itself reports an error.  This call synchronises the stream. */
+cpa_status cpa_last_device_error(void *stream);
+
+/* Static description of a status code. */
+const char *cpa_status_string(cpa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t cpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPA_H_ */

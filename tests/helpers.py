@@ -1,0 +1,130 @@
+"""Shared helpers for the GPU parity tests: run a workload through the CUDA
+library and through the fp64 oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+
+BF16_ATOL = 2e-2   # max-abs error bound for BF16 outputs against the fp64 oracle
+FP32_ATOL = 1e-4   # max-abs error bound for FP32 outputs
+BF16_LSE_ATOL = 2e-3
+FP32_LSE_ATOL = 1e-4
+BF16_REL_RMS = 1e-2  # diagnostic gate on relative RMS error
+
+
+def to_oracle(t: torch.Tensor) -> np.ndarray:
+    """float32 values, or bfloat16 bit patterns as uint16."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(t.dtype)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy()
+    return t.view(torch.int32).numpy()
+
+
+def params_for(w: W.Workload, flags=None, kv_segment_size=None, timeout_cycles=0):
+    import chunked_prefill_paged_gb300 as cpa
+    sh = w.shape
+    return cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                      sh.kv_segment_size if kv_segment_size is None else kv_segment_size, sh.scale,
+                      cpa.DTYPE_FP32 if sh.dtype == "f32" else cpa.DTYPE_BF16,
+                      cpa.FLAG_FUSE_KV_WRITE if flags is None else flags, timeout_cycles)
+
+
+def sample_rows(step: W.Step, n_per_req: int, seed: int) -> List[int]:
+    """First and last token of every request plus random ones (sorted, unique)."""
+    rng = np.random.default_rng(seed)
+    cu = step.cu_new_tokens
+    rows = set()
+    for r in range(len(step.num_new_tokens)):
+        a, b = int(cu[r]), int(cu[r + 1])
+        if b <= a:
+            continue
+        rows.update([a, b - 1])
+        k = min(n_per_req, b - a)
+        rows.update(int(x) for x in rng.integers(a, b, size=k))
+    return sorted(rows)
+
+
+class Result:
+    def __init__(self):
+        self.max_err = 0.0
+        self.max_lse_err = 0.0
+        self.rel_rms = []
+        self.rows_checked = 0
+
+    def add(self, gpu_out: np.ndarray, ref_out: np.ndarray, gpu_lse: Optional[np.ndarray], ref_lse: np.ndarray):
+        assert np.all(np.isfinite(gpu_out)), "non-finite output"
+        err = np.abs(gpu_out.astype(np.float64) - ref_out)
+        self.max_err = max(self.max_err, float(err.max()) if err.size else 0.0)
+        if err.size:
+            self.rel_rms.append(float(np.sqrt((err ** 2).mean()) / max(np.sqrt((ref_out ** 2).mean()), 1e-30)))
+        if gpu_lse is not None and gpu_lse.size:
+            self.max_lse_err = max(self.max_lse_err, float(np.abs(gpu_lse.astype(np.float64) - ref_lse).max()))
+        self.rows_checked += gpu_out.shape[0]
+
+
+def run_and_compare(w: W.Workload, *, flags=None, kv_segment_size=None, rows_per_req: Optional[int] = None,
+                    steps_to_check: Optional[Sequence[int]] = None, threads=None, check_pool=True,
+                    seed: int = 0, device="cuda"):
+    """Run every step of `w` on the GPU (fused K/V write unless flags say
+    otherwise, then the standalone write) and in the oracle; compare the
+    checked steps' outputs (all rows, or a sample) and the final pool."""
+    import chunked_prefill_paged_gb300 as cpa
+    sh = w.shape
+    t = w.materialize(device)
+    k_pool_o = to_oracle(t.k_cache)
+    v_pool_o = to_oracle(t.v_cache)
+    params = params_for(w, flags, kv_segment_size)
+    fused = bool(params.flags & cpa.FLAG_FUSE_KV_WRITE)
+    res = Result()
+    steps_to_check = range(len(w.steps)) if steps_to_check is None else steps_to_check
+    for si, step in enumerate(w.steps):
+        batch = cpa.Batch(step.cached_seq_len, step.num_new_tokens, w.block_table, device=device)
+        q, kn, vn = t.step_inputs(step)
+        out, lse = cpa.attention(batch, params, q, kn, vn, t.k_cache, t.v_cache)
+        if not fused:
+            cpa.paged_kv_write(batch, params, kn, vn, t.k_cache, t.v_cache)
+        torch.cuda.synchronize()
+        ob = oracle.Batch(step.cached_seq_len, step.num_new_tokens, w.block_table)
+        qo, kno, vno = to_oracle(q), to_oracle(kn), to_oracle(vn)
+        if si in steps_to_check and step.total_new_tokens > 0:
+            rows = None if rows_per_req is None else sample_rows(step, rows_per_req, seed + si)
+            ref_o, ref_l = oracle.attention(ob, qo, kno, vno, k_pool_o, v_pool_o, num_heads_q=sh.num_heads_q,
+                                            num_heads_kv=sh.num_heads_kv, head_dim=sh.head_dim,
+                                            block_size=sh.block_size, scale=sh.scale, rows=rows,
+                                            threads=threads)
+            idx = slice(None) if rows is None else torch.as_tensor(rows, device=out.device)
+            res.add(out[idx].float().cpu().numpy(), ref_o, lse[idx].cpu().numpy(), ref_l)
+        k_pool_o, v_pool_o = oracle.kv_write(ob, kno, vno, k_pool_o, v_pool_o, num_heads_kv=sh.num_heads_kv,
+                                             head_dim=sh.head_dim, block_size=sh.block_size)
+    if check_pool:
+        assert np.array_equal(bits(t.k_cache), k_pool_o.view(np.int16 if sh.dtype == "bf16" else np.int32)), \
+            "K pool differs from the oracle's write"
+        assert np.array_equal(bits(t.v_cache), v_pool_o.view(np.int16 if sh.dtype == "bf16" else np.int32)), \
+            "V pool differs from the oracle's write"
+    assert cpa.last_device_error() == cpa.SUCCESS
+    return res
+
+
+def assert_within(res: Result, dtype: str):
+    if dtype == "f32":
+        assert res.max_err <= FP32_ATOL, f"max-abs error {res.max_err:.3e} > {FP32_ATOL}"
+        assert res.max_lse_err <= FP32_LSE_ATOL, f"lse error {res.max_lse_err:.3e}"
+    else:
+        assert res.max_err <= BF16_ATOL, f"max-abs error {res.max_err:.3e} > {BF16_ATOL}"
+        assert res.max_lse_err <= BF16_LSE_ATOL, f"lse error {res.max_lse_err:.3e}"
+        assert max(res.rel_rms) <= BF16_REL_RMS, f"relative RMS error {max(res.rel_rms):.3e}"

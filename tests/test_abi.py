@@ -1,0 +1,133 @@
+"""The C ABI library on the CPU: it loads, exports every function declared in
+include/*.h, and its host-side checks reject bad arguments before any launch
+(no GPU is touched by these calls)."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_prefill_paged_gb300 import build
+    build.build()
+    import chunked_prefill_paged_gb300 as cpa
+    return cpa
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    names.discard("defined")
+    return names
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert {"paged_kv_write", "chunked_prefill_attention", "chunked_prefill_workspace_size"} <= names
+    handle = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(handle, n), f"{n} declared in include/ but not exported"
+    assert set(lib.EXPORTED) <= names
+
+
+def test_version_and_status_strings(lib):
+    L = lib.load()
+    assert L.cpa_version() >= 100
+    for s in range(7):
+        assert lib.status_string(s)
+
+
+def _cbatch(lib, cached, new, max_blocks, dev_ptr=0x1000):
+    h_c = np.asarray(cached, dtype=np.int32)
+    h_n = np.asarray(new, dtype=np.int32)
+    b = lib.binding._Batch(len(h_c), max_blocks, int(h_n.sum()), dev_ptr, dev_ptr, dev_ptr, dev_ptr,
+                           h_c.ctypes.data, h_n.ctypes.data)
+    return b, (h_c, h_n)
+
+
+BAD_PARAMS = [
+    dict(num_heads_q=30, num_heads_kv=8),    # H_q not a multiple of H_kv
+    dict(head_dim=96),
+    dict(block_size=8),
+    dict(kv_segment_size=768),
+    dict(kv_segment_size=512, block_size=128, num_blocks=0),
+    dict(dtype=5),
+    dict(scale=float("inf")),
+]
+
+
+@pytest.mark.parametrize("bad", BAD_PARAMS)
+def test_bad_params_rejected_before_launch(lib, bad):
+    kw = dict(num_heads_q=32, num_heads_kv=8, head_dim=128, block_size=16, num_blocks=100, kv_segment_size=1024)
+    kw.update(bad)
+    p = lib.Params(**kw).c()
+    b, keep = _cbatch(lib, [10], [5], 4)
+    L = lib.load()
+    rc = L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0, None)
+    assert rc == lib.ERR_INVALID_ARG
+    rc = L.paged_kv_write(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, None)
+    assert rc == lib.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cached,new,max_blocks", [
+    ([10], [-1], 4),          # negative length
+    ([-3], [2], 4),
+    ([60], [5], 4),           # C + N beyond the block table (4 x 16)
+])
+def test_bad_batches_rejected(lib, cached, new, max_blocks):
+    p = lib.Params(32, 8, 128, 16, 100, 1024).c()
+    b, keep = _cbatch(lib, cached, new, max_blocks)
+    L = lib.load()
+    assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0,
+                                       None) == lib.ERR_INVALID_ARG
+
+
+def test_total_tokens_must_match(lib):
+    p = lib.Params(32, 8, 128, 16, 100, 1024).c()
+    b, keep = _cbatch(lib, [3, 4], [5, 6], 4)
+    b.total_new_tokens = 12
+    L = lib.load()
+    assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0,
+                                       None) == lib.ERR_INVALID_ARG
+
+
+def test_misaligned_pointer_rejected(lib):
+    p = lib.Params(32, 8, 128, 16, 100, 1024).c()
+    b, keep = _cbatch(lib, [3], [5], 4)
+    L = lib.load()
+    assert L.paged_kv_write(ctypes.byref(b), ctypes.byref(p), 18, 16, 16, 16, None) == lib.ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    p = lib.Params(32, 8, 128, 16, 100, 1024).c()
+    b = lib.binding._Batch(0, 1, 0, None, None, None, None, None, None)
+    L = lib.load()
+    assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), None, None, None, None, None, None, None,
+                                       None, 0, None) == lib.SUCCESS
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == 0
+
+
+def test_workspace_size_counts_split_partials(lib):
+    L = lib.load()
+    # 3 decodes (one row group of G = 4 rows each), H_kv 8, d 128, split 1024
+    p = lib.Params(32, 8, 128, 16, 10000, 1024).c()
+    b, keep = _cbatch(lib, [5000, 100, 2047], [1, 1, 1], 400)
+    pieces = [-(-(5000 + 1) // 1024), 1, -(-(2047 + 1) // 1024)]
+    expect = sum(8 * n * 4 * (128 + 2) * 4 for n in pieces if n > 1)
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == expect
+    # no split requested: no workspace
+    p2 = lib.Params(32, 8, 128, 16, 10000, 1024, flags=lib.FLAG_NO_SPLIT).c()
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p2)) == 0
+    # a prefill chunk of 512 tokens spans many query tiles and is never split
+    b3, keep3 = _cbatch(lib, [8000], [512], 600)
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b3), ctypes.byref(p)) == 0

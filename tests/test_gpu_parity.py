@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded
+inputs, through the C ABI.  BF16 outputs within max-abs 2e-2 (plus a relative
+RMS gate of 1e-2), FP32 within 1e-4; the paged K/V pool bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import (BF16_ATOL, assert_within, bits, params_for, run_and_compare, to_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cpa():
+    import chunked_prefill_paged_gb300 as m
+    m.load()
+    return m
+
+
+def small_batch(hq=8, hkv=2, d=128, bs=16, dtype="bf16", seg=512, reqs=None, seed=7):
+    reqs = reqs or [(0, 300), (130, 77), (1000, 1), (17, 1), (257, 129), (0, 0), (64, 0), (5, 3)]
+    return W.make_batch_workload(f"small_{hq}_{hkv}_{d}_{bs}_{dtype}", W.Shape(hq, hkv, d, bs, seg, dtype), reqs,
+                                 seed=seed)
+
+
+# ------------------------------------------------------------------ KV write
+@pytest.mark.parametrize("dtype,bs,d", [("bf16", 16, 128), ("bf16", 128, 128), ("f32", 16, 64), ("bf16", 32, 64)])
+def test_paged_kv_write_bit_exact(cpa, dtype, bs, d):
+    w = small_batch(d=d, bs=bs, dtype=dtype)
+    t = w.materialize("cuda")
+    s = w.steps[0]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+    p = params_for(w)
+    q, kn, vn = t.step_inputs(s)
+    k_ref, v_ref = oracle.kv_write(oracle.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table),
+                                   to_oracle(kn), to_oracle(vn), to_oracle(t.k_cache), to_oracle(t.v_cache),
+                                   num_heads_kv=w.shape.num_heads_kv, head_dim=d, block_size=bs)
+    cpa.paged_kv_write(b, p, kn, vn, t.k_cache, t.v_cache)
+    torch.cuda.synchronize()
+    vt = np.int16 if dtype == "bf16" else np.int32
+    assert np.array_equal(bits(t.k_cache), k_ref.view(vt))
+    assert np.array_equal(bits(t.v_cache), v_ref.view(vt))
+    assert cpa.last_device_error() == cpa.SUCCESS
+
+
+# ------------------------------------------------------- small, every row
+def test_tiny_fp32_config(cpa):
+    w = W.tiny_fp32()
+    res = run_and_compare(w)
+    assert_within(res, "f32")
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 16), (8, 2, 128, 128), (8, 1, 128, 32), (16, 2, 64, 64),
+                                         (4, 4, 128, 16), (32, 4, 128, 16)])
+def test_small_batch_tensor_cores(cpa, hq, hkv, d, bs):
+    w = small_batch(hq, hkv, d, bs)
+    res = run_and_compare(w)
+    assert_within(res, "bf16")
+
+
+def test_small_batch_cuda_cores_bf16(cpa):
+    w = small_batch()
+    res = run_and_compare(w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_FORCE_SIMT)
+    assert_within(res, "bf16")
+
+
+def test_small_batch_fp32_cuda_cores(cpa):
+    w = small_batch(d=64, dtype="f32")
+    res = run_and_compare(w)
+    assert_within(res, "f32")
+
+
+@pytest.mark.parametrize("seg", [512, 1024, 2048, 4096])
+def test_split_kv_decodes_every_segment_size(cpa, seg):
+    reqs = [(5000, 1), (4095, 1), (4096, 1), (777, 1), (9000, 3), (0, 1), (1, 1), (2300, 16)]
+    w = small_batch(reqs=reqs, seg=seg, seed=11)
+    res = run_and_compare(w, kv_segment_size=seg)
+    assert_within(res, "bf16")
+
+
+def test_no_split_matches_split(cpa):
+    reqs = [(5000, 1), (3000, 2), (123, 1)]
+    w = small_batch(reqs=reqs, seed=12)
+    res = run_and_compare(w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_NO_SPLIT)
+    assert_within(res, "bf16")
+
+
+def test_standalone_write_then_read_only_attention(cpa):
+    w = small_batch(seed=13)
+    res = run_and_compare(w, flags=0)
+    assert_within(res, "bf16")
+
+
+def test_chunked_prompt_multistep_fused_write(cpa):
+    sh = W.Shape(16, 4, 128, 16, 512, "bf16")
+    w = W.make_prompt_workload("prompt700", sh, 700, 256, 64, seed=14)
+    res = run_and_compare(w)
+    assert_within(res, "bf16")
+
+
+def test_first_token_of_fresh_prompt_returns_its_value_row(cpa):
+    # C = 0: token 0 sees only itself, p = 1, l = 1, so out = v_0 exactly
+    w = small_batch(reqs=[(0, 40), (0, 1)], seed=15)
+    t = w.materialize("cuda")
+    s = w.steps[0]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+    q, kn, vn = t.step_inputs(s)
+    out, _ = cpa.attention(b, params_for(w), q, kn, vn, t.k_cache, t.v_cache)
+    G = w.shape.num_heads_q // w.shape.num_heads_kv
+    for tok in (0, 40):
+        for h in range(w.shape.num_heads_q):
+            assert torch.equal(out[tok, h], vn[tok, h // G])
+
+
+def test_chunking_invariance_on_gpu(cpa):
+    # the same prompt in one chunk and in uneven chunks gives the same output
+    sh = W.Shape(8, 2, 128, 16, 512, "bf16")
+    outs = []
+    for chunk in (600, 200, 137):
+        w = W.make_prompt_workload("inv", sh, 600, chunk, 64, seed=16)
+        t = w.materialize("cuda")
+        p = params_for(w)
+        rows = []
+        for step in w.steps:
+            b = cpa.Batch(step.cached_seq_len, step.num_new_tokens, w.block_table)
+            q, kn, vn = t.step_inputs(step)
+            o, _ = cpa.attention(b, p, q, kn, vn, t.k_cache, t.v_cache)
+            rows.append(o.float())
+        outs.append(torch.cat(rows))
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2 * BF16_ATOL
+
+
+# ------------------------------------------------------------ edge cases
+def test_empty_batch_and_zero_token_requests(cpa):
+    w = small_batch(reqs=[(10, 0), (0, 0)], seed=17)
+    t = w.materialize("cuda")
+    s = w.steps[0]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+    q = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    before = bits(t.k_cache)
+    cpa.chunked_prefill_attention(b, params_for(w), q, kv, kv, t.k_cache, t.v_cache, out)
+    cpa.paged_kv_write(b, params_for(w), kv, kv, t.k_cache, t.v_cache)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(t.k_cache), before)
+
+
+def test_invalid_arguments_are_rejected(cpa):
+    w = small_batch(seed=18)
+    t = w.materialize("cuda")
+    s = w.steps[0]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+    q, kn, vn = t.step_inputs(s)
+    out = torch.empty_like(q)
+    bad = params_for(w, kv_segment_size=768)
+    with pytest.raises(cpa.CpaError) as e:
+        cpa.chunked_prefill_attention(b, bad, q, kn, vn, t.k_cache, t.v_cache, out)
+    assert e.value.status == cpa.ERR_INVALID_ARG
+    decodes = small_batch(reqs=[(5000, 1)], seed=19)
+    td = decodes.materialize("cuda")
+    sd = decodes.steps[0]
+    bd = cpa.Batch(sd.cached_seq_len, sd.num_new_tokens, decodes.block_table)
+    qd, knd, vnd = td.step_inputs(sd)
+    with pytest.raises(cpa.CpaError) as e:
+        cpa.chunked_prefill_attention(bd, params_for(decodes), qd, knd, vnd, td.k_cache, td.v_cache,
+                                      torch.empty_like(qd))
+    assert e.value.status == cpa.ERR_WORKSPACE
+
+
+# ------------------------------------------- the measured workloads, sampled
+def test_config_llama3_8b_prompt(cpa):
+    res = run_and_compare(W.llama3_8b_prompt(), rows_per_req=24)
+    assert_within(res, "bf16")
+
+
+def test_config_prefix_cache(cpa):
+    res = run_and_compare(W.prefix_cache(), rows_per_req=4)
+    assert_within(res, "bf16")
+
+
+def test_config_mixed_step(cpa):
+    res = run_and_compare(W.mixed_step(), rows_per_req=3)
+    assert_within(res, "bf16")
+
+
+def test_config_long_context(cpa):
+    res = run_and_compare(W.long_context(), rows_per_req=6, steps_to_check=[0, 7, 15])
+    assert_within(res, "bf16")
