@@ -39,6 +39,11 @@ constexpr int kErrBadBlock = 5;
 
 CPA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Floats of one split unit's partial: output [rows][d], then the row maxima
+// [rows] and sums [rows], padded to a multiple of 4 floats so that every
+// unit's output block starts 16-byte aligned.
+CPA_HD long long partial_floats(int rows, int d) { return (long long)rows * d + ((2 * rows + 3) & ~3); }
+
 struct ReqWork {
     int direct_units;    // H_kv * query tiles, or 0
     int split_units;     // H_kv * pieces, or 0
@@ -56,7 +61,7 @@ CPA_HD ReqWork request_work(int C, int N, int G, int hkv, int d, int tile_m, int
         if (pieces > 1) {
             w.split_units = hkv * pieces;
             w.pieces = pieces;
-            w.ws_floats = (long long)w.split_units * rows * (d + 2);
+            w.ws_floats = (long long)w.split_units * partial_floats(rows, d);
             return w;
         }
     }

@@ -94,7 +94,7 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
                 u.rows = rows_total;
                 u.k_begin = u.piece * a.split_len;
                 u.k_end = min(u.k_begin + a.split_len, u.C + u.N);
-                u.ws_off = wsb + (long long)local * rows_total * (a.d + 2);
+                u.ws_off = wsb + (long long)local * partial_floats(rows_total, a.d);
             }
             return true;
         }

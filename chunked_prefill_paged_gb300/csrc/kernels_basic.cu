@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     if (r < 0) return;
     const int N = __ldg(a.nnew + r), cu0 = __ldg(a.cu + r);
     const int rows = N * a.G;
-    const long long unit_floats = (long long)rows * (D + 2);
+    const long long unit_floats = partial_floats(rows, D);
     T *out = static_cast<T *>(a.out);
     for (int lr = warp; lr < rows; lr += 4) {
         float M = -INFINITY;
