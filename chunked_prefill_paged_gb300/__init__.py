@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     Params,
     attention,
     chunked_prefill_attention,
+    chunked_prefill_attention_no_alloc,
     last_device_error,
     load,
     paged_kv_write,

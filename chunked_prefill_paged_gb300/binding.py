@@ -74,6 +74,7 @@ EXPORTED = [
     "chunked_prefill_workspace_size",
     "paged_kv_write",
     "chunked_prefill_attention",
+    "chunked_prefill_attention_no_alloc",
     "cpa_last_device_error",
     "cpa_status_string",
     "cpa_version",
@@ -99,6 +100,8 @@ def load(path: str = LIB_PATH):
     lib.chunked_prefill_attention.restype = ctypes.c_int
     lib.chunked_prefill_attention.argtypes = [P(_Batch), P(_Params), VP, VP, VP, VP, VP, VP, VP, VP,
                                               ctypes.c_size_t, VP]
+    lib.chunked_prefill_attention_no_alloc.restype = ctypes.c_int
+    lib.chunked_prefill_attention_no_alloc.argtypes = [P(_Batch), P(_Params), VP, VP, VP, VP, VP, VP, VP, VP]
     lib.cpa_last_device_error.restype = ctypes.c_int
     lib.cpa_last_device_error.argtypes = [VP]
     lib.cpa_status_string.restype = ctypes.c_char_p
@@ -208,6 +211,19 @@ def chunked_prefill_attention(batch: Batch, params: Params, q, k_new, v_new, k_c
                                           ws_bytes, _stream_ptr(stream))
     if rc != SUCCESS:
         raise CpaError(rc, "chunked_prefill_attention")
+
+
+def chunked_prefill_attention_no_alloc(batch: Batch, params: Params, q, k_new, v_new, k_cache, v_cache, out,
+                                       lse=None, stream=None) -> None:
+    """chunked_prefill_attention without a workspace argument: for callers
+    that cannot allocate device memory; the library's static device array
+    holds the split-KV partials (see include/cpa.h)."""
+    b, p = batch.c(), params.c()
+    rc = load().chunked_prefill_attention_no_alloc(ctypes.byref(b), ctypes.byref(p), _ptr(q), _ptr(k_new),
+                                                   _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                                   _ptr(lse), _stream_ptr(stream))
+    if rc != SUCCESS:
+        raise CpaError(rc, "chunked_prefill_attention_no_alloc")
 
 
 def last_device_error(stream=None) -> int:

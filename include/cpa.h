@@ -155,6 +155,32 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
                                      void *v_cache, void *out, float *lse, void *workspace,
                                      size_t workspace_bytes, void *stream);
 
+/* Bytes of the static device array behind chunked_prefill_attention_no_alloc. */
+#define CPA_NO_ALLOC_WORKSPACE_BYTES (32u << 20)
+
+/* chunked_prefill_attention for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is a calling convenience.)  Some
+ * callers cannot call cudaMalloc and have no spare device buffer to lend as
+ * workspace -- a plugin inside a host application that owns all device memory
+ * through its own pool, or a serving loop that must not call cudaMalloc /
+ * cudaFree because they can synchronise the device.  This call takes the same
+ * arguments minus the workspace and allocates nothing: the split-KV partials
+ * go to one file-scope device array of CPA_NO_ALLOC_WORKSPACE_BYTES that every
+ * GPU loading the library holds until the process exits.
+ *   - A batch whose partials need more than that (see
+ *     chunked_prefill_workspace_size) returns CPA_ERR_WORKSPACE and launches
+ *     nothing.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; nothing in it has to start at zero.  Calls that overlap on the
+ *     GPU (e.g. on two streams at once) race on it: serialise them.
+ *   - The first call on a device looks up the array's device address and
+ *     caches it; make that first call before any stream capture.
+ * Results are those of chunked_prefill_attention on the same inputs. */
+cpa_status chunked_prefill_attention_no_alloc(const cpa_batch *batch, const cpa_params *params,
+                                              const void *q, const void *k_new, const void *v_new,
+                                              void *k_cache, void *v_cache, void *out, float *lse,
+                                              void *stream);
+
 /* Wait for `stream`, then return and clear the first error recorded by a
  * kernel on the current device since the last call (CPA_SUCCESS if none):
  * CPA_ERR_DEVICE_TIMEOUT or CPA_ERR_BAD_BLOCK_ID.  CPA_ERR_CUDA if the
