@@ -81,7 +81,7 @@ cpa_status validate(const cpa_batch *b, const cpa_params *p) {
     const int ks = p->kv_segment_size;
     if (ks != 0 && ks != 512 && ks != 1024 && ks != 2048 && ks != 4096) return CPA_ERR_INVALID_ARG;
     if (ks != 0 && ks % p->block_size != 0) return CPA_ERR_INVALID_ARG;
-    if (!isfinite(p->scale)) return CPA_ERR_INVALID_ARG;
+    if (!isfinite(p->scale) || !(p->scale > 0.f)) return CPA_ERR_INVALID_ARG;
     if (p->timeout_cycles < 0) return CPA_ERR_INVALID_ARG;
     if (b->num_reqs < 0 || b->total_new_tokens < 0) return CPA_ERR_INVALID_ARG;
     if (b->num_reqs == 0) return b->total_new_tokens == 0 ? CPA_SUCCESS : CPA_ERR_INVALID_ARG;
@@ -110,6 +110,7 @@ bool use_tensor_cores(const cpa_params *p) {
 
 struct Plan {
     int tile_m = 0;
+    int tiles_per_unit = 1;
     int split_len = 0;
     int direct_units = 0;
     int split_units = 0;
@@ -119,12 +120,14 @@ struct Plan {
 
 Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     Plan pl;
-    pl.tile_m = use_tensor_cores(p) ? kTcTileM : kSimtTileM;
+    const bool tc = use_tensor_cores(p);
+    pl.tile_m = tc ? kTcTileM : kSimtTileM;
+    pl.tiles_per_unit = 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     const int G = p->num_heads_q / p->num_heads_kv;
     for (int r = 0; r < b->num_reqs; ++r) {
         const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
-                                       p->head_dim, pl.tile_m, pl.split_len);
+                                       p->head_dim, pl.tile_m, pl.split_len, pl.tiles_per_unit);
         pl.direct_units += w.direct_units;
         pl.split_units += w.split_units;
         pl.split_reqs += w.split_units > 0 ? 1 : 0;
@@ -167,7 +170,9 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
     {
         const cuuint64_t dims[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
         const cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
-        const cuuint32_t box[4] = {64, 1, (cuuint32_t)bs, 1};
+        // one box is one block, or the half of a 128-token block that one key tile covers
+        const cuuint32_t box_rows = (cuuint32_t)(bs < (cuuint64_t)kTcTileN ? bs : (cuuint64_t)kTcTileN);
+        const cuuint32_t box[4] = {64, 1, box_rows, 1};
         if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims, strides, box)) return s;
         if (cpa_status s = encode(&m.v_pool, v_cache, 4, dims, strides, box)) return s;
     }
@@ -263,6 +268,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.scale_log2 = params->scale * 1.4426950408889634f;
     a.split_len = pl.split_len;
     a.tile_m = pl.tile_m;
+    a.tiles_per_unit = pl.tiles_per_unit;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
     a.q = q;
@@ -274,7 +280,9 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.lse = lse;
     a.ws = static_cast<float *>(workspace);
     a.fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) ? 1 : 0;
-    a.write_ctas = pl.direct_units + pl.split_units;
+    const int units = pl.direct_units + pl.split_units;
+    // the tensor-core kernel is persistent: at most one CTA per SM
+    a.write_ctas = (pl.tile_m == kTcTileM) ? (units < dev.sms ? units : dev.sms) : units;
     a.err = dev.err;
     a.timeout_cycles = params->timeout_cycles > 0 ? params->timeout_cycles : kDefaultTimeoutCycles;
     a.test_stall = (params->flags & CPA_FLAG_TEST_STALL) ? 1 : 0;

@@ -13,7 +13,7 @@
 //     of "Prefill Processing" (Kernel Interface, Partial KV Segment
 //     Handling) -- each written as a partial (unnormalised output, max,
 //     sum) and merged by attn_merge.
-// Direct units are numbered first (heaviest query tile of each request
+// Direct units are numbered first (the heaviest query tiles of each request
 // first), then split units.  Host and device both use request_work() so the
 // launch size and the device-side decode agree.
 #pragma once
@@ -29,7 +29,7 @@
 namespace cpa {
 
 constexpr int kTcTileM = 128;    // packed query rows per tensor-core tile
-constexpr int kTcTileN = 128;    // keys per K/V tile
+constexpr int kTcTileN = 128;    // keys per K/V tile of the tensor-core kernel
 constexpr int kSimtTileM = 16;   // packed query rows per CUDA-core tile
 constexpr int kDefaultSplit = 1024;
 
@@ -51,7 +51,9 @@ struct ReqWork {
     long long ws_floats; // floats of partials for a split request
 };
 
-CPA_HD ReqWork request_work(int C, int N, int G, int hkv, int d, int tile_m, int split_len) {
+// tiles_per_unit: query tiles one direct unit covers (the tensor-core kernel
+// pairs two consecutive tiles of a request so they share every K/V tile).
+CPA_HD ReqWork request_work(int C, int N, int G, int hkv, int d, int tile_m, int split_len, int tiles_per_unit) {
     ReqWork w{0, 0, 0, 0};
     if (N <= 0) return w;
     const int rows = N * G;
@@ -65,7 +67,7 @@ CPA_HD ReqWork request_work(int C, int N, int G, int hkv, int d, int tile_m, int
             return w;
         }
     }
-    w.direct_units = hkv * n_qt;
+    w.direct_units = hkv * cdiv(n_qt, tiles_per_unit);
     return w;
 }
 
@@ -84,6 +86,7 @@ struct AttnArgs {
     float scale_log2;  // softmax scale * log2(e)
     int split_len;     // 0: no split units
     int tile_m;
+    int tiles_per_unit; // query tiles per direct unit
     int num_direct_units;
     int num_split_units;
     // data

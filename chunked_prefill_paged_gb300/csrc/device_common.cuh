@@ -32,7 +32,8 @@ __device__ __forceinline__ int request_of_token(const int32_t *cu, int num_reqs,
 struct Unit {
     int r, g, qt, piece;  // piece < 0: direct unit
     int C, N, cu0;
-    int row0, rows;       // packed rows [row0, row0 + rows) of the request
+    int row0, rows;       // packed rows [row0, row0 + rows) of the request (up to
+                          // tiles_per_unit * tile_m rows)
     int k_begin, k_end;   // keys [k_begin, k_end) of this unit
     long long ws_off;     // float offset of the unit's partial (split units)
 };
@@ -49,7 +50,7 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
         const int r = r0 + lane;
         ReqWork w{0, 0, 0, 0};
         if (r < a.num_reqs) w = request_work(__ldg(a.cached + r), __ldg(a.nnew + r), a.G, a.hkv, a.d, a.tile_m,
-                                             a.split_len);
+                                             a.split_len, a.tiles_per_unit);
         const int cnt = split ? w.split_units : w.direct_units;
         const long long wsf = split ? w.ws_floats : 0;
         int inc = cnt;
@@ -78,11 +79,15 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
             u.g = local % a.hkv;
             const int rows_total = u.N * a.G;
             if (!split) {
+                // unit i of a request covers query tiles [last - tiles_per_unit + 1, last]
+                // with last = n_qt - 1 - i * tiles_per_unit: heaviest tiles first
                 const int n_qt = cdiv(rows_total, a.tile_m);
-                u.qt = n_qt - 1 - local / a.hkv;  // heaviest tile of the request first
+                const int last = n_qt - 1 - (local / a.hkv) * a.tiles_per_unit;
+                const int first = max(0, last - a.tiles_per_unit + 1);
+                u.qt = first;
                 u.piece = -1;
-                u.row0 = u.qt * a.tile_m;
-                u.rows = min(a.tile_m, rows_total - u.row0);
+                u.row0 = first * a.tile_m;
+                u.rows = min((last + 1) * a.tile_m, rows_total) - u.row0;
                 const int last_tok = (u.row0 + u.rows - 1) / a.G;
                 u.k_begin = 0;
                 u.k_end = u.C + last_tok + 1;

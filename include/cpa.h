@@ -114,7 +114,7 @@ typedef struct {
                                  block_size ("Prefill Processing", Kernel Interface).  It is the
                                  unit in which the keys of single-tile requests (decodes) are
                                  split across CTAs and merged. */
-    float scale;              /* softmax scale applied to q.k (usually 1/sqrt(d)) */
+    float scale;              /* softmax scale applied to q.k, finite and > 0 (usually 1/sqrt(d)) */
     int32_t dtype;            /* cpa_dtype */
     uint32_t flags;           /* CPA_FLAG_* */
     int64_t timeout_cycles;   /* bound of every device-side wait, in SM clock cycles;

@@ -63,6 +63,7 @@ BAD_PARAMS = [
     dict(kv_segment_size=512, block_size=128, num_blocks=0),
     dict(dtype=5),
     dict(scale=float("inf")),
+    dict(scale=-0.1),
 ]
 
 
