@@ -24,15 +24,19 @@
 //              holds up the next K copy.  A pool tile is one box per cache
 //              block (found through the block table), a new-token tile one
 //              128-row box of k_new / v_new.  Warp 11 idles.
-//   warp 9     MMA issuer (converged; one elected lane issues).  Scores run one tile ahead: for key tile
-//              j it issues S(j+1) = Q K(j+1)^T into the other score buffer,
-//              then O += P(j) V(j) once the softmax has written P(j), so the
-//              tensor core computes the next scores while softmax runs.
+//   warp 9     MMA issuer (converged; one elected lane issues).  Scores run
+//              two tiles ahead: for key tile j it issues S(j+2) = Q K(j+2)^T
+//              into a free score buffer, then O += P(j) V(j) once the
+//              softmax has written P(j), so the tensor core computes the next
+//              scores while softmax runs.
 //
-// TMEM (512 columns): two score buffers S0 [0,128) and S1 [128,256), O
-// [256, 256 + D).  P(j), as bf16 pairs, overwrites the first 64 columns of
-// the buffer that held S(j); S(j+2) reuses that buffer only after PV(j) was
-// issued (tensor-core ops from one thread run in order).  Rescaling is lazy:
+// TMEM (512 columns): three score buffers S0 [0,128), S1 [128,256) and
+// S2 [256,384), O [384, 384 + D).  P(j), as bf16 pairs, overwrites the first
+// 64 columns of the buffer that held S(j); S(j+3) reuses that buffer only
+// after PV(j) was issued (tensor-core ops from one thread run in order).
+// With three buffers the scores run two tiles ahead of the softmax, so the
+// chain softmax(j) -> PV(j) -> S(j+3) -> softmax(j+3) spans two other
+// softmax tiles instead of one.  Rescaling is lazy:
 // a row's reference maximum moves (and O is rescaled, after waiting for the
 // previous PV) only when a tile's maximum exceeds it by more than 2^8 in the
 // exp2 domain; the final O / l is exact whichever reference was used.
@@ -58,6 +62,8 @@ constexpr int kProducerWarp = 8;      // Q and K copies
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;    // V copies (warp 11 idles)
 constexpr int kKT = kTcTileN;         // keys per K/V tile (128)
+constexpr int kSBuf = 3;              // score buffers in TMEM
+constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -74,8 +80,8 @@ struct __align__(8) TcShared {
     uint64_t q_full, q_empty;
     uint64_t k_full[6], k_empty[6];
     uint64_t v_full[6], v_empty[6];
-    uint64_t s_full[2];  // per score buffer
-    uint64_t p_full[2];  // per score buffer: P(j) written over S(j)
+    uint64_t s_full[kSBuf];  // per score buffer
+    uint64_t p_full[kSBuf];  // per score buffer: P(j) written over S(j)
     uint64_t pv_done;
     uint64_t o_full, o_empty;
     uint64_t mma_done;
@@ -88,6 +94,38 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+// 2^x for a pair of arguments on the FMA pipe instead of the MUFU unit,
+// by Cody-Waite range reduction and a polynomial: x = n + f with n the
+// nearest integer (the 1.5 * 2^23 rounding constant) and f in [-1/2, 1/2];
+// 2^f comes from a degree-3 polynomial fitted here for minimax relative
+// error (Lawson's iteratively reweighted least squares; max relative error
+// 7.5e-5, well under bf16's 2^-9), and 2^n is added to the exponent field.
+// Arguments below -126 are clamped there, which yields a value of at most
+// 2^-125 in place of the exact (smaller) one.
+constexpr float kExp2C0 = 0.99992809f;
+constexpr float kExp2C1 = 0.69326099f;
+constexpr float kExp2C2 = 0.24261081f;
+constexpr float kExp2C3 = 0.05517144f;
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -126.0f);
+    x.y = fmaxf(x.y, -126.0f);
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));       // n in the low mantissa bits
+    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));     // n as a float
+    const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);      // x - n
+    float2 p = __ffma2_rn(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+    p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
+    p = __ffma2_rn(p, f, make_float2(kExp2C0, kExp2C0));
+    // (bits of t) << 23 == n << 23 modulo 2^32: the constant's own bits shift out
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
+#ifndef CPA_POLY_PAIRS
+#define CPA_POLY_PAIRS 0  // of the 32 exponential pairs per thread and tile
+#endif
+__host__ __device__ constexpr bool poly_pair(int i) { return (i * CPA_POLY_PAIRS) % 32 < CPA_POLY_PAIRS; }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -163,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.v_full[s], 1);
             mbar_init(&sh.v_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kSBuf; ++b) {
             mbar_init(&sh.s_full[b], 1);
             mbar_init(&sh.p_full[b], kSoftmaxThreads);
         }
@@ -194,10 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ================================================================ TMA
         const int kv_role = (warp == kVProducerWarp) ? 1 : 0;  // copies K (0) or V (1)
-        long long gt = 0;  // key tiles of the units before this one
-        int it = 0;        // units started by this CTA
+        int it = 0;  // units started by this CTA
         bool ok = true;
-        long long issued = 0;  // tiles (counted in gt) whose copies this warp issued
+        const int ns = kv_role ? NSV : NSK;
+        int slot = 0;         // ring slot of the next copy
+        uint32_t ph = 0;      // parity of that slot's current fill
+        int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x, ++it) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
@@ -211,13 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *bt_row = a.bt + (long long)u.r * a.max_blocks;
             // copies of key tile j (K when kv = 0, V when kv = 1) into their ring slot
             auto load_kv = [&](int j, int kv) -> bool {
-                const long long g = gt + j;
-                const int ns = kv ? NSV : NSK;
-                const int st = (int)(g % ns);
-                const uint32_t ph = (uint32_t)((g / ns) & 1);
-                uint64_t *empty = kv ? &sh.v_empty[st] : &sh.k_empty[st];
-                uint64_t *full = kv ? &sh.v_full[st] : &sh.k_full[st];
-                uint8_t *dst = (kv ? sV : sK) + st * TB;
+                uint64_t *empty = kv ? &sh.v_empty[slot] : &sh.k_empty[slot];
+                uint64_t *full = kv ? &sh.v_full[slot] : &sh.k_full[slot];
+                uint8_t *dst = (kv ? sV : sK) + slot * TB;
                 if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1u, LIM)) || __any_sync(0xffffffffu, *abort_flag))
                     return false;
                 int key0, valid;
@@ -249,7 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane < Cfg::kHalves)
                         tma_load_3d(dst + lane * HB, kv ? &tm_v_new : &tm_k_new, full, lane * 64, u.g, row);
                 }
-                issued = g + 1;
+                if (++slot == ns) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+                if (pending < ns) ++pending;
                 return true;
             };
             if (kv_role == 0) {
@@ -268,37 +308,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 1);
             }
-            gt += n;
         }
         if (!ok) {
             if (lane == 0) record_error(a.err, kErrTimeout);
             *abort_flag = 1;
         }
-        // drain: every issued copy must land before the CTA may exit
-        {
-            const int ns = kv_role ? NSV : NSK;
-            for (long long g = (issued > ns ? issued - ns : 0); g < issued; ++g)
-                mbar_wait(kv_role ? &sh.v_full[(int)(g % ns)] : &sh.k_full[(int)(g % ns)], (uint32_t)((g / ns) & 1),
-                          LIM);
+        // drain: every issued copy must land before the CTA may exit.  The
+        // last `pending` fills occupy the slots just before `slot`.
+        for (int i = pending; i >= 1; --i) {
+            int st = slot - i;
+            uint32_t p = ph;
+            if (st < 0) {
+                st += ns;
+                p ^= 1u;
+            }
+            mbar_wait(kv_role ? &sh.v_full[st] : &sh.k_full[st], p, LIM);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA
-        long long gt = 0;
         int qcnt = 0;  // units started
-        int gs = 0;    // score tiles issued (buffer gs & 1)
-        int pc = 0;    // P tiles consumed
+        int sb = 0, pb = 0;          // score buffer of the next S issue and of the next P consumed
+        uint32_t sph = 0, pph = 0;   // use parity of those buffers
         int oc = 0;    // units finished
+        int ks = 0, vs = 0;          // ring slots of the next K and V tiles
+        uint32_t kph = 0, vph = 0;   // and the parity of their fill
         bool ok = true;
         constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-        // Shared-memory descriptors are built once; a k-step or ring slot only
-        // advances the start-address field (bytes >> 4), which stays below 2^14
-        // for any shared-memory address.
+        // Shared-memory descriptors: the high halves (stride, version,
+        // swizzle) are common to Q, K and V; only the low halves (start
+        // address >> 4 and leading byte offset) differ.  Addresses stay below
+        // 2^18 bytes, so adding (bytes >> 4) never carries out of the field.
         const uint64_t q_desc = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
-        const uint64_t k_desc0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
-        const uint64_t v_desc0 = smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
-        const uint32_t tO = tmem + 256;
+        const uint32_t desc_hi = (uint32_t)(q_desc >> 32);
+        const uint32_t q_lo = (uint32_t)q_desc;
+        const uint32_t k_lo0 = (uint32_t)smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
+        const uint32_t v_lo0 = (uint32_t)smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
+        const uint32_t tO = tmem + kTmemO;
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
@@ -310,65 +357,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA and commit, and every wait is taken by all lanes.
             // S(jj) = Q K(jj)^T into the next score buffer
             auto issue_s = [&](int jj) -> bool {
-                const long long g = gt + jj;
-                const int st = (int)(g % NSK);
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.k_full[st], (uint32_t)((g / NSK) & 1), LIM)) ||
+                if (!__all_sync(0xffffffffu, mbar_wait(&sh.k_full[ks], kph, LIM)) ||
                     __any_sync(0xffffffffu, *abort_flag))
                     return false;
                 tc_fence_after();
-                const uint64_t kd = k_desc0 + (uint64_t)((st * TB) >> 4);
-                const uint32_t d_tmem = tmem + (gs & 1) * kKT;
+                const uint32_t k_lo = k_lo0 + (uint32_t)ks * (uint32_t)(TB >> 4);
+                const uint32_t d_tmem = tmem + sb * kKT;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
-                    umma_ss_warp(d_tmem, q_desc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
+                    umma_ss_warp2(d_tmem, q_lo + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit_warp(&sh.s_full[gs & 1]);
-                umma_commit_warp(&sh.k_empty[st]);
-                ++gs;
+                umma_commit_warp(&sh.s_full[sb]);
+                umma_commit_warp(&sh.k_empty[ks]);
+                if (++sb == kSBuf) {
+                    sb = 0;
+                    sph ^= 1u;
+                }
+                if (++ks == NSK) {
+                    ks = 0;
+                    kph ^= 1u;
+                }
                 if (jj == n - 1) umma_commit_warp(&sh.q_empty);  // Q is free once the last S is done
                 return true;
             };
             if (!__all_sync(0xffffffffu, mbar_wait(&sh.q_full, (uint32_t)(qcnt++ & 1), LIM))) ok = false;
             tc_fence_after();
             if (ok) ok = issue_s(0);
+            if (ok && n > 1) ok = issue_s(1);
             for (int j = 0; j < n && ok; ++j) {
                 // the next scores go first, into the buffer PV(j-1) has finished reading
-                if (j + 1 < n && !issue_s(j + 1)) {
+                if (j + 2 < n && !issue_s(j + 2)) {
                     ok = false;
                     break;
                 }
-                const int b = pc & 1;  // P(j) sits in the buffer S(j) used
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.p_full[b], (uint32_t)((pc >> 1) & 1), LIM))) {
+                const int b = pb;  // P(j) sits in the buffer S(j) used
+                if (!__all_sync(0xffffffffu, mbar_wait(&sh.p_full[b], pph, LIM))) {
                     ok = false;
                     break;
                 }
-                ++pc;
+                if (++pb == kSBuf) {
+                    pb = 0;
+                    pph ^= 1u;
+                }
                 if (j == 0 && !__all_sync(0xffffffffu, mbar_wait(&sh.o_empty, (uint32_t)((oc & 1) ^ 1), LIM))) {
                     ok = false;
                     break;
                 }
-                const long long g = gt + j;
-                const int st = (int)(g % NSV);
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.v_full[st], (uint32_t)((g / NSV) & 1), LIM))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sh.v_full[vs], vph, LIM))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t vd = v_desc0 + (uint64_t)((st * TB) >> 4);
+                const uint32_t v_lo = v_lo0 + (uint32_t)vs * (uint32_t)(TB >> 4);
                 const uint32_t tP = tmem + b * kKT;
 #pragma unroll
                 for (int kk = 0; kk < kKT / 16; ++kk)
-                    umma_ts_warp(tO, tP + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_pv,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit_warp(&sh.v_empty[st]);
+                    umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_warp(&sh.v_empty[vs]);
                 umma_commit_warp(&sh.pv_done);
+                if (++vs == NSV) {
+                    vs = 0;
+                    vph ^= 1u;
+                }
                 if (j == n - 1) {
                     umma_commit_warp(&sh.o_full);
                     ++oc;
                 }
             }
-            gt += n;
         }
         if (!ok) {
             if (lane == 0) record_error(a.err, kErrTimeout);
@@ -384,10 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lr = 32 * (warp & 3) + 16 * (warp >> 2) + (lane & 15);  // row of the tile == TMEM lane
         if (a.fuse_write) fused_write_share(a, blockIdx.x, gridDim.x, tid, kSoftmaxThreads, 2);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3) + 16 * (warp >> 2)) << 16);
-        const uint32_t tO = lane_base + 256;
+        const uint32_t tO = lane_base + kTmemO;
         const float sl = a.scale_log2;
         long long gt = 0;
         int gs = 0;  // score tiles consumed (== P tiles produced)
+        int cb = 0;          // score buffer of the next tile
+        uint32_t cph = 0;    // and its use parity
         int oc = 0;
         bool ok = true;
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
@@ -401,13 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos = row_valid ? u.C + (u.row0 + lr) / a.G : -1;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                const int b = gs & 1;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&sh.s_full[b], (uint32_t)((gs >> 1) & 1), LIM) && !*abort_flag)) {
+                const int b = cb;
+                if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], cph, LIM) && !*abort_flag)) {
                     ok = false;
                     break;
                 }
                 ++gs;
+                if (++cb == kSBuf) {
+                    cb = 0;
+                    cph ^= 1u;
+                }
                 tc_fence_after();
                 const uint32_t tS = lane_base + b * kKT;
                 int key0, valid;
@@ -451,25 +513,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= alpha;
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
                 {
+                    // exponentials in pairs: most on the MUFU unit, the pairs
+                    // poly_pair() picks on the FMA pipe, so that neither unit
+                    // alone sets the pace
                     uint32_t r[32];
+                    const float2 sl2 = make_float2(sl, sl), neg2 = make_float2(neg, neg);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2(fmaf(s[2 * i], sl, neg));
-                        const float e1 = ex2(fmaf(s[2 * i + 1], sl, neg));
-                        if (i & 1) {
-                            a2 += e0;
-                            a3 += e1;
+                        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sl2, neg2);
+                        float2 e;
+                        if (poly_pair(i)) {
+                            e = exp2_poly2(x);
                         } else {
-                            a0 += e0;
-                            a1 += e1;
+                            e.x = ex2(x.x);
+                            e.y = ex2(x.y);
                         }
-                        r[i] = pack_bf16(e0, e1);
+                        if (i & 1)
+                            acc1 = __fadd2_rn(acc1, e);
+                        else
+                            acc0 = __fadd2_rn(acc0, e);
+                        r[i] = pack_bf16(e.x, e.y);
                     }
                     tmem_st16x2_32<32>(tS, r);  // threads 0-15: P columns 0-31, 16-31: 32-63
                 }
-                l += (a0 + a1) + (a2 + a3);
+                l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 if (j >= 1 && __any_sync(0xffffffffu, move)) {
                     // rescale O once PV(j-1) (global P tile gs - 2) has completed;
                     // PV(j) cannot start before this group's arrival below
