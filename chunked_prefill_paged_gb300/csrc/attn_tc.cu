@@ -254,8 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t *empty = kv ? &sh.v_empty[slot] : &sh.k_empty[slot];
                 uint64_t *full = kv ? &sh.v_full[slot] : &sh.k_full[slot];
                 uint8_t *dst = (kv ? sV : sK) + slot * TB;
-                if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1u, LIM)) || __any_sync(0xffffffffu, *abort_flag))
-                    return false;
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(empty, ph ^ 1u, LIM, abort_flag))) return false;
                 int key0, valid;
                 bool pooled;
                 tl.tile(j, key0, valid, pooled);
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the first K tile does not depend on the Q buffer: issue it
                 // before waiting for the previous unit's last score MMA
                 ok = load_kv(0, 0);
-                if (ok && it > 0 && !__all_sync(0xffffffffu, mbar_wait(&sh.q_empty, (uint32_t)((it - 1) & 1), LIM)))
+                if (ok && it > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty, (uint32_t)((it - 1) & 1), LIM, abort_flag)))
                     ok = false;
                 if (ok) {
                     if (lane == 0) mbar_arrive_expect_tx(&sh.q_full, TB);
@@ -357,9 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA and commit, and every wait is taken by all lanes.
             // S(jj) = Q K(jj)^T into the next score buffer
             auto issue_s = [&](int jj) -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.k_full[ks], kph, LIM)) ||
-                    __any_sync(0xffffffffu, *abort_flag))
-                    return false;
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.k_full[ks], kph, LIM, abort_flag))) return false;
                 tc_fence_after();
                 const uint32_t k_lo = k_lo0 + (uint32_t)ks * (uint32_t)(TB >> 4);
                 const uint32_t d_tmem = tmem + sb * kKT;
@@ -381,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (jj == n - 1) umma_commit_warp(&sh.q_empty);  // Q is free once the last S is done
                 return true;
             };
-            if (!__all_sync(0xffffffffu, mbar_wait(&sh.q_full, (uint32_t)(qcnt++ & 1), LIM))) ok = false;
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_full, (uint32_t)(qcnt++ & 1), LIM, abort_flag))) ok = false;
             tc_fence_after();
             if (ok) ok = issue_s(0);
             if (ok && n > 1) ok = issue_s(1);
@@ -392,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int b = pb;  // P(j) sits in the buffer S(j) used
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.p_full[b], pph, LIM))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.p_full[b], pph, LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -400,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pb = 0;
                     pph ^= 1u;
                 }
-                if (j == 0 && !__all_sync(0xffffffffu, mbar_wait(&sh.o_empty, (uint32_t)((oc & 1) ^ 1), LIM))) {
+                if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_empty, (uint32_t)((oc & 1) ^ 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.v_full[vs], vph, LIM))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[vs], vph, LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -461,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 const int b = cb;
-                if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], cph, LIM) && !*abort_flag)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.s_full[b], cph, LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -542,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j >= 1 && __any_sync(0xffffffffu, move)) {
                     // rescale O once PV(j-1) (global P tile gs - 2) has completed;
                     // PV(j) cannot start before this group's arrival below
-                    if (!__all_sync(0xffffffffu, mbar_wait(&sh.pv_done, (uint32_t)((gs - 2) & 1), LIM))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.pv_done, (uint32_t)((gs - 2) & 1), LIM, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -561,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // keys past the tile's valid range: zero their V rows so that
                     // P = 0 never meets a NaN or Inf left in the pool or in smem
                     const long long g = gt + j;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&sh.v_full[(int)(g % NSV)], (uint32_t)((g / NSV) & 1), LIM))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[(int)(g % NSV)],
+                                                                    (uint32_t)((g / NSV) & 1), LIM, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -578,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&sh.p_full[b]);
             }
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sh.o_full, (uint32_t)(oc & 1), LIM));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_full, (uint32_t)(oc & 1), LIM, abort_flag));
             if (!ok) break;
             tc_fence_after();
             l += __shfl_xor_sync(0xffffffffu, l, 16);  // whole row

@@ -58,6 +58,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     return true;
 }
 
+// As mbar_wait, and also gives up (returns false) once *abort is set.  The
+// flag is read only while the phase is still open, so a wait on a phase
+// that has already completed costs one try_wait.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, long long limit,
+                                                   const volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
 // ------------------------------------------------------- register budget
 // Move registers between warpgroups of a running CTA (every warp of the
 // warpgroup executes it).  `dec` returns registers to the CTA's pool, `inc`
