@@ -23,20 +23,19 @@
 //              tiles, each into its own ring, so a V slot still in use never
 //              holds up the next K copy.  A pool tile is one box per cache
 //              block (found through the block table), a new-token tile one
-//              128-row box of k_new / v_new.  Warp 11 idles.
-//   warp 9     MMA issuer (converged; one elected lane issues).  Scores run
-//              two tiles ahead: for key tile j it issues S(j+2) = Q K(j+2)^T
-//              into a free score buffer, then O += P(j) V(j) once the
-//              softmax has written P(j), so the tensor core computes the next
-//              scores while softmax runs.
+//              128-row box of k_new / v_new.
+//   warp 9     score MMA issuer: S(j) = Q K(j)^T into score buffer j % 3 as
+//              soon as K(j) is in and the PV that last read that buffer has
+//              completed, so scores run up to three tiles ahead of the PVs.
+//   warp 11    PV MMA issuer: O += P(j) V(j) once the softmax has written P(j).
+//              Issuing from two warps on different SM sub-partitions halves
+//              the instruction stream each shares with the softmax warps.
 //
 // TMEM (512 columns): three score buffers S0 [0,128), S1 [128,256) and
 // S2 [256,384), O [384, 384 + D).  P(j), as bf16 pairs, overwrites the first
 // 64 columns of the buffer that held S(j); S(j+3) reuses that buffer only
-// after PV(j) was issued (tensor-core ops from one thread run in order).
-// With three buffers the scores run two tiles ahead of the softmax, so the
-// chain softmax(j) -> PV(j) -> S(j+3) -> softmax(j+3) spans two other
-// softmax tiles instead of one.  Rescaling is lazy:
+// after PV(j) has completed.  With three buffers the chain softmax(j) ->
+// PV(j) -> S(j+3) -> softmax(j+3) spans two other softmax tiles.  Rescaling is lazy:
 // a row's reference maximum moves (and O is rescaled, after waiting for the
 // previous PV) only when a tile's maximum exceeds it by more than 2^8 in the
 // exp2 domain; the final O / l is exact whichever reference was used.
@@ -60,7 +59,8 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;      // Q and K copies
 constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;    // V copies (warp 11 idles)
+constexpr int kVProducerWarp = 10;    // V copies
+constexpr int kPvWarp = 11;           // PV MMA issuer
 constexpr int kKT = kTcTileN;         // keys per K/V tile (128)
 constexpr int kSBuf = 3;              // score buffers in TMEM
 constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
@@ -82,7 +82,7 @@ struct __align__(8) TcShared {
     uint64_t v_full[6], v_empty[6];
     uint64_t s_full[kSBuf];  // per score buffer
     uint64_t p_full[kSBuf];  // per score buffer: P(j) written over S(j)
-    uint64_t pv_done;
+    uint64_t pv_done[kSBuf];  // per score buffer: the PV that read its P has completed
     uint64_t o_full, o_empty;
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -205,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.s_full[b], 1);
             mbar_init(&sh.p_full[b], kSoftmaxThreads);
         }
-        mbar_init(&sh.pv_done, 1);
+        for (int b = 0; b < kSBuf; ++b) mbar_init(&sh.pv_done[b], 1);
         mbar_init(&sh.o_full, 1);
         mbar_init(&sh.o_empty, kSoftmaxThreads);
-        mbar_init(&sh.mma_done, 1);
+        mbar_init(&sh.mma_done, 2);  // one commit from each MMA warp
         sh.abort_flag = 0;
         fence_mbar_init();
     }
@@ -324,14 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(kv_role ? &sh.v_full[st] : &sh.k_full[st], p, LIM);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kPvWarp) {
         // ================================================================ MMA
-        int qcnt = 0;  // units started
-        int sb = 0, pb = 0;          // score buffer of the next S issue and of the next P consumed
-        uint32_t sph = 0, pph = 0;   // use parity of those buffers
-        int oc = 0;    // units finished
-        int ks = 0, vs = 0;          // ring slots of the next K and V tiles
-        uint32_t kph = 0, vph = 0;   // and the parity of their fill
+        // Two issuing warps on different SM sub-partitions: warp 9 issues the
+        // score MMAs, warp 11 the PV MMAs.  Each runs converged; one elected
+        // lane issues each MMA and commit, and every wait is taken by all
+        // lanes.  A score buffer is reused only once the PV that read its P
+        // has completed (pv_done of that buffer).
+        int ub = 0;                  // score buffer of this warp's next tile
+        uint32_t uph = 0;            // use parity of that buffer
+        int rs = 0;                  // ring slot (K for warp 9, V for warp 11)
+        uint32_t rph = 0;            // and the parity of its fill
+        long long issued = 0;        // tiles issued by this warp
+        int ucnt = 0;                // units started
         bool ok = true;
         constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
@@ -345,90 +350,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_lo0 = (uint32_t)smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
         const uint32_t v_lo0 = (uint32_t)smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
         const uint32_t tO = tmem + kTmemO;
-        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
+        const bool s_role = (warp == kMmaWarp);
+        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x, ++ucnt) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
             TileList tl;
             tl.init(u);
             const int n = tl.n_total;
-            // The whole warp runs this converged; one elected lane issues each
-            // MMA and commit, and every wait is taken by all lanes.
-            // S(jj) = Q K(jj)^T into the next score buffer
-            auto issue_s = [&](int jj) -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.k_full[ks], kph, LIM, abort_flag))) return false;
-                tc_fence_after();
-                const uint32_t k_lo = k_lo0 + (uint32_t)ks * (uint32_t)(TB >> 4);
-                const uint32_t d_tmem = tmem + sb * kKT;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
-                    umma_ss_warp2(d_tmem, q_lo + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                umma_commit_warp(&sh.s_full[sb]);
-                umma_commit_warp(&sh.k_empty[ks]);
-                if (++sb == kSBuf) {
-                    sb = 0;
-                    sph ^= 1u;
-                }
-                if (++ks == NSK) {
-                    ks = 0;
-                    kph ^= 1u;
-                }
-                if (jj == n - 1) umma_commit_warp(&sh.q_empty);  // Q is free once the last S is done
-                return true;
-            };
-            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_full, (uint32_t)(qcnt++ & 1), LIM, abort_flag))) ok = false;
-            tc_fence_after();
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
-            for (int j = 0; j < n && ok; ++j) {
-                // the next scores go first, into the buffer PV(j-1) has finished reading
-                if (j + 2 < n && !issue_s(j + 2)) {
-                    ok = false;
-                    break;
-                }
-                const int b = pb;  // P(j) sits in the buffer S(j) used
-                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.p_full[b], pph, LIM, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                if (++pb == kSBuf) {
-                    pb = 0;
-                    pph ^= 1u;
-                }
-                if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_empty, (uint32_t)((oc & 1) ^ 1), LIM, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[vs], vph, LIM, abort_flag))) {
+            if (s_role) {
+                // S(j) = Q K(j)^T, as far ahead as the score buffers allow
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_full, (uint32_t)(ucnt & 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t v_lo = v_lo0 + (uint32_t)vs * (uint32_t)(TB >> 4);
-                const uint32_t tP = tmem + b * kKT;
+                for (int j = 0; j < n; ++j) {
+                    if (issued >= kSBuf &&
+                        !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.pv_done[ub], uph ^ 1u, LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.k_full[rs], rph, LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_lo = k_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
+                    const uint32_t d_tmem = tmem + ub * kKT;
 #pragma unroll
-                for (int kk = 0; kk < kKT / 16; ++kk)
-                    umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit_warp(&sh.v_empty[vs]);
-                umma_commit_warp(&sh.pv_done);
-                if (++vs == NSV) {
-                    vs = 0;
-                    vph ^= 1u;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
+                        umma_ss_warp2(d_tmem, q_lo + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit_warp(&sh.s_full[ub]);
+                    umma_commit_warp(&sh.k_empty[rs]);
+                    if (j == n - 1) umma_commit_warp(&sh.q_empty);  // Q is free once the last S is done
+                    ++issued;
+                    if (++ub == kSBuf) {
+                        ub = 0;
+                        uph ^= 1u;
+                    }
+                    if (++rs == NSK) {
+                        rs = 0;
+                        rph ^= 1u;
+                    }
                 }
-                if (j == n - 1) {
-                    umma_commit_warp(&sh.o_full);
-                    ++oc;
+            } else {
+                // O += P(j) V(j) once the softmax has written P(j)
+                for (int j = 0; j < n; ++j) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.p_full[ub], uph, LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_empty, (uint32_t)((ucnt & 1) ^ 1),
+                                                                               LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[rs], rph, LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t v_lo = v_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
+                    const uint32_t tP = tmem + ub * kKT;
+#pragma unroll
+                    for (int kk = 0; kk < kKT / 16; ++kk)
+                        umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
+                                      (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_warp(&sh.v_empty[rs]);
+                    umma_commit_warp(&sh.pv_done[ub]);
+                    if (j == n - 1) umma_commit_warp(&sh.o_full);
+                    if (++ub == kSBuf) {
+                        ub = 0;
+                        uph ^= 1u;
+                    }
+                    if (++rs == NSV) {
+                        rs = 0;
+                        rph ^= 1u;
+                    }
                 }
+                if (!ok) break;
             }
         }
         if (!ok) {
             if (lane == 0) record_error(a.err, kErrTimeout);
             *abort_flag = 1;
         }
-        // every MMA issued so far must finish before TMEM is freed
+        // every MMA issued so far (by both warps) must finish before TMEM is freed
         umma_commit_warp(&sh.mma_done);
         mbar_wait(&sh.mma_done, 0, LIM);
         __syncwarp();
@@ -441,9 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = lane_base + kTmemO;
         const float sl = a.scale_log2;
         long long gt = 0;
-        int gs = 0;  // score tiles consumed (== P tiles produced)
         int cb = 0;          // score buffer of the next tile
         uint32_t cph = 0;    // and its use parity
+        int prev_b = 0;      // buffer and use parity of the previous tile (for the PV(j-1) wait)
+        uint32_t prev_ph = 0;
         int oc = 0;
         bool ok = true;
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
@@ -458,11 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 const int b = cb;
+                const uint32_t bph = cph;
                 if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.s_full[b], cph, LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
-                ++gs;
                 if (++cb == kSBuf) {
                     cb = 0;
                     cph ^= 1u;
@@ -537,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 if (j >= 1 && __any_sync(0xffffffffu, move)) {
-                    // rescale O once PV(j-1) (global P tile gs - 2) has completed;
-                    // PV(j) cannot start before this group's arrival below
-                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.pv_done, (uint32_t)((gs - 2) & 1), LIM, abort_flag))) {
+                    // rescale O once PV(j-1) has completed; PV(j) cannot start
+                    // before this group's arrival below
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.pv_done[prev_b], prev_ph, LIM, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -574,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.p_full[b]);
+                prev_b = b;
+                prev_ph = bph;
             }
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_full, (uint32_t)(oc & 1), LIM, abort_flag));
             if (!ok) break;
