@@ -1,6 +1,6 @@
 // attn_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) attention over the paged
 // K/V cache for BF16.  Persistent: one CTA per SM walks the work units (see
-// cpa_internal.h) in order blockIdx.x, blockIdx.x + gridDim.x, ...
+// cpa_internal.h) in serpentine order (unit_of_round).
 //
 // What a unit computes ("Prefill Processing", How Segmentation Works with KV
 // Segments, Kernel Interface, Partial KV Segment Handling; "Prefill
@@ -167,6 +167,14 @@ struct TileList {
     }
 };
 
+// The unit a CTA takes in its round r of the persistent loop.  Rounds
+// alternate direction (serpentine), so that with the units of a request
+// ordered heaviest first every CTA ends up with a similar amount of work.
+__device__ __forceinline__ int unit_of_round(int r) {
+    const int b = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    return r * (int)gridDim.x + b;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
         int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
-        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x, ++it) {
+        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++it)) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_lo0 = (uint32_t)smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
         const uint32_t tO = tmem + kTmemO;
         const bool s_role = (warp == kMmaWarp);
-        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x, ++ucnt) {
+        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++ucnt)) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -457,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t prev_ph = 0;
         int oc = 0;
         bool ok = true;
-        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
+        int round = 0;
+        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++round)) {
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
