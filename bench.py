@@ -13,6 +13,15 @@ oracle timed on the host cores, the SM clocks seen during the timed region,
 and a secondary line for the decode-heavy mixed step (KV-read GB/s).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py --case NAME [--steps K --warmup W]
+
+--case times one attention call of a single workload step (for profiling
+under ncu and per-configuration timing) and prints {"case": ..., "ms": ...}:
+  llama_chunk        last 1808-token chunk of the Llama-3-8B prompt (bs 128)
+  long_context_last  last 2048-token chunk of the 32,768-token prompt
+                     (H_q 64, bs 16, cached 30,720)
+  mixed_step         64 decodes + 512-token chunks under a 2048 budget
+  prefix_cache       16 requests sharing a 4096-token cached prefix
 """
 from __future__ import annotations
 
@@ -40,6 +49,15 @@ METRIC = "chunk-attn TFLOP/s (algorithmic, visible pairs only)"
 UNIT = "TFLOP/s"
 
 
+# name -> (workload constructor, step index)
+CASES = {
+    "llama_chunk": (W.llama3_8b_prompt, -1),
+    "long_context_last": (W.long_context, -1),
+    "mixed_step": (W.mixed_step, 0),
+    "prefix_cache": (W.prefix_cache, 0),
+}
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -49,6 +67,8 @@ def parse_args():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="time one attention call of this workload step instead of the bench step")
     return ap.parse_args()
 
 
@@ -355,6 +375,49 @@ def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush):
             "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy"}
 
 
+def run_case(args, local):
+    """One attention call of one workload step, timed with CUDA events after
+    an L2 flush; for profiling and per-configuration numbers."""
+    import chunked_prefill_paged_gb300 as cpa
+    from chunked_prefill_paged_gb300 import build
+    build.build()
+    cpa.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    make, idx = CASES[args.case]
+    w = make()
+    sh = w.shape
+    t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
+    s = w.steps[idx]
+    params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16 if sh.dtype == "bf16" else cpa.DTYPE_FP32,
+                        cpa.FLAG_FUSE_KV_WRITE)
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
+    q, k, v = t.step_inputs(s)
+    out = torch.empty_like(q)
+    n = cpa.workspace_size(b, params)
+    ws = torch.empty(max(n // 4, 4), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError("device error")
+    ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
+    i = idx % len(w.steps)
+    flops, byts = w.flops_per_step()[i], w.bytes_per_step()[i]
+    return {"case": args.case, "workload": w.name, "steps": args.steps, "warmup": args.warmup, "ms": round(ms, 4),
+            "tflops": round(flops / (ms / 1e3) / 1e12, 1), "gbs": round(byts / (ms / 1e3) / 1e9, 1),
+            "flops": flops, "bytes": byts, "tokens": int(s.total_new_tokens)}
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands on the host cores, same metric and workload;
     each step a bounded sample."""
@@ -391,7 +454,9 @@ def run_reference(args, rank, world):
 def main():
     args = parse_args()
     rank, world, local = dist_setup()
-    if args.impl == "reference":
+    if args.case is not None:
+        line = run_case(args, local) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world, local)

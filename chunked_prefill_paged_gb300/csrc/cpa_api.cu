@@ -111,12 +111,15 @@ bool use_tensor_cores(const cpa_params *p) {
 struct Plan {
     int tile_m = 0;
     int tiles_per_unit = 1;
+    int head_major = 0;
     int split_len = 0;
     int direct_units = 0;
     int split_units = 0;
     int split_reqs = 0;
     long long ws_floats = 0;
 };
+
+int elem_bytes(const cpa_params *p) { return p->dtype == CPA_DTYPE_FP32 ? 4 : 2; }
 
 Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     Plan pl;
@@ -125,6 +128,7 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     pl.tiles_per_unit = 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     const int G = p->num_heads_q / p->num_heads_kv;
+    double kv_bytes = 0;
     for (int r = 0; r < b->num_reqs; ++r) {
         const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
                                        p->head_dim, pl.tile_m, pl.split_len, pl.tiles_per_unit);
@@ -132,11 +136,15 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
         pl.split_units += w.split_units;
         pl.split_reqs += w.split_units > 0 ? 1 : 0;
         pl.ws_floats += w.ws_floats;
+        kv_bytes += (double)(b->h_cached_seq_len[r] + b->h_num_new_tokens[r]) * p->num_heads_kv * p->head_dim * 2.0 *
+                    elem_bytes(p);
     }
+    // K/V of the batch larger than about half of L2: walk the direct units
+    // head by head so that concurrent CTAs share K/V tiles in L2
+    pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
     return pl;
 }
 
-int elem_bytes(const cpa_params *p) { return p->dtype == CPA_DTYPE_FP32 ? 4 : 2; }
 
 cpa_status encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                   const cuuint32_t *box) {
@@ -269,6 +277,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.split_len = pl.split_len;
     a.tile_m = pl.tile_m;
     a.tiles_per_unit = pl.tiles_per_unit;
+    a.head_major = pl.head_major;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
     a.q = q;

@@ -32,6 +32,9 @@ constexpr int kTcTileM = 128;    // packed query rows per tensor-core tile
 constexpr int kTcTileN = 128;    // keys per K/V tile of the tensor-core kernel
 constexpr int kSimtTileM = 16;   // packed query rows per CUDA-core tile
 constexpr int kDefaultSplit = 1024;
+// Batches whose K/V (all requests, cached + new) exceed this many bytes walk
+// their direct units kv head by kv head (about half of GB300's L2).
+constexpr double kHeadMajorKvBytes = 64.0 * 1024 * 1024;
 
 // device error codes (match cpa_status)
 constexpr int kErrTimeout = 4;
@@ -87,6 +90,8 @@ struct AttnArgs {
     int split_len;     // 0: no split units
     int tile_m;
     int tiles_per_unit; // query tiles per direct unit
+    int head_major;     // direct units of a request ordered kv head by kv head
+                        // (else kv head innermost); see decode_unit
     int num_direct_units;
     int num_split_units;
     // data

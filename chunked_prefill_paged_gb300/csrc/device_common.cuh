@@ -79,10 +79,21 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
             u.g = local % a.hkv;
             const int rows_total = u.N * a.G;
             if (!split) {
-                // unit i of a request covers query tiles [last - tiles_per_unit + 1, last]
-                // with last = n_qt - 1 - i * tiles_per_unit: heaviest tiles first
+                // the request's i-th tile group of kv head g covers query tiles
+                // [last - tiles_per_unit + 1, last] with last = n_qt - 1 -
+                // i * tiles_per_unit: heaviest tiles first.  Kv head innermost
+                // (local = i * hkv + g) spreads concurrent CTAs over all heads,
+                // which balances causal chunks best; head-major (local = g *
+                // groups + i) keeps concurrent CTAs on one or two heads' K/V,
+                // which keeps the working set in L2 for long contexts.
                 const int n_qt = cdiv(rows_total, a.tile_m);
-                const int last = n_qt - 1 - (local / a.hkv) * a.tiles_per_unit;
+                const int groups = cdiv(n_qt, a.tiles_per_unit);
+                int i = local / a.hkv;
+                if (a.head_major) {
+                    u.g = local / groups;
+                    i = local - u.g * groups;
+                }
+                const int last = n_qt - 1 - i * a.tiles_per_unit;
                 const int first = max(0, last - a.tiles_per_unit + 1);
                 u.qt = first;
                 u.piece = -1;
