@@ -151,16 +151,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+KERNEL_SOURCES = ("attn_tc.cu", "device_common.cuh", "ptx_sm100.cuh", "cpa_internal.h", "cpa_api.cu")
+
+
+def kernel_sources_sha256() -> str:
+    """One hash over the sources the attention kernel and its launch are built from."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "chunked_prefill_paged_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def kernel_traffic_record():
     """dram bytes per launch of the attention kernel from the committed ncu
-    summary, only if the kernel source has not changed since the capture."""
+    summary, only if none of the kernel's sources changed since the capture."""
     p = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
-    src = os.path.join(ROOT, "chunked_prefill_paged_gb300", "csrc", "attn_tc.cu")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if rec.get("attn_tc_sha256") != h:
+    if rec.get("sources_sha256") != kernel_sources_sha256():
         return None
     return rec
 
