@@ -1,6 +1,8 @@
 // attn_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) attention over the paged
-// K/V cache for BF16.  Persistent: one CTA per SM walks the work units (see
-// cpa_internal.h) in serpentine order (unit_of_round).
+// K/V cache for BF16.  Persistent: one CTA per SM takes work units (see
+// cpa_internal.h) from a per-launch counter in the workspace, in index
+// order (a request's heaviest units first), so that CTAs that finish early
+// take more units.
 //
 // What a unit computes ("Prefill Processing", How Segmentation Works with KV
 // Segments, Kernel Interface, Partial KV Segment Handling; "Prefill
@@ -65,19 +67,22 @@ constexpr int kKT = kTcTileN;         // keys per K/V tile (128)
 constexpr int kSBuf = 3;              // score buffers in TMEM
 constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kUnitRing = 4;                // unit indices passed ahead to the other roles
+constexpr int kUnitReaders = 11;            // warps 0-7, 9, 10, 11 each read every index
 
 template <int D>
 struct TcCfg {
     static constexpr int kHalves = D / 64;           // 64-element (128 B) column chunks
     static constexpr int kTileBytes = 128 * D * 2;   // 128 rows of D bf16 (Q, K or V tile)
     static constexpr int kHalfBytes = kTileBytes / kHalves;
+    static constexpr int kQStages = 2;  // the next unit's Q loads while this one runs
     static constexpr int kKStages = (D == 128) ? 3 : 6;
-    static constexpr int kVStages = (D == 128) ? 3 : 6;
-    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (1 + kKStages + kVStages);
+    static constexpr int kVStages = (D == 128) ? 2 : 5;
+    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages);
 };
 
 struct __align__(8) TcShared {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[6], k_empty[6];
     uint64_t v_full[6], v_empty[6];
     uint64_t s_full[kSBuf];  // per score buffer
@@ -85,6 +90,10 @@ struct __align__(8) TcShared {
     uint64_t pv_done[kSBuf];  // per score buffer: the PV that read its P has completed
     uint64_t o_full, o_empty;
     uint64_t mma_done;
+    // unit scheduler: warp 8 takes unit indices from the launch's work
+    // counter and passes them to the other roles through this ring
+    uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
+    int unit_ring[kUnitRing];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -167,12 +176,18 @@ struct TileList {
     }
 };
 
-// The unit a CTA takes in its round r of the persistent loop.  Rounds
-// alternate direction (serpentine), so that with the units of a request
-// ordered heaviest first every CTA ends up with a similar amount of work.
-__device__ __forceinline__ int unit_of_round(int r) {
-    const int b = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-    return r * (int)gridDim.x + b;
+// The i-th unit of this CTA, as published by the scheduling warp (every lane
+// of the calling warp takes part).  Returns a value >= the unit count when
+// the CTA is done, and -1 when the wait gave up (timeout or abort).
+__device__ __forceinline__ int read_unit(TcShared &sh, int i, long long limit, const volatile int *abort_flag) {
+    const int s = i % kUnitRing;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.unit_full[s], (uint32_t)((i / kUnitRing) & 1), limit,
+                                                    abort_flag)))
+        return -1;
+    const int unit = *reinterpret_cast<volatile int *>(&sh.unit_ring[s]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.unit_empty[s]);
+    return unit;
 }
 
 template <int D>
@@ -188,8 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcShared sh;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sQ = smem;
-    uint8_t *sK = smem + TB;           // NSK stages
+    uint8_t *sQ = smem;                // 2 stages
+    uint8_t *sK = smem + Cfg::kQStages * TB;  // NSK stages
     uint8_t *sV = sK + NSK * TB;       // NSV stages
 
     const int tid = threadIdx.x;
@@ -199,8 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total_units = a.num_direct_units + a.num_split_units;
 
     if (tid == 0) {
-        mbar_init(&sh.q_full, 1);
-        mbar_init(&sh.q_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.q_full[b], 1);
+            mbar_init(&sh.q_empty[b], 1);
+        }
         for (int s = 0; s < NSK; ++s) {
             mbar_init(&sh.k_full[s], 1);
             mbar_init(&sh.k_empty[s], 1);
@@ -217,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sh.o_full, 1);
         mbar_init(&sh.o_empty, kSoftmaxThreads);
         mbar_init(&sh.mma_done, 2);  // one commit from each MMA warp
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(&sh.unit_full[i], 1);
+            mbar_init(&sh.unit_empty[i], kUnitReaders);
+        }
         sh.abort_flag = 0;
         fence_mbar_init();
     }
@@ -240,13 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ================================================================ TMA
         const int kv_role = (warp == kVProducerWarp) ? 1 : 0;  // copies K (0) or V (1)
-        int it = 0;  // units started by this CTA
         bool ok = true;
         const int ns = kv_role ? NSV : NSK;
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
         int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
-        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++it)) {
+        // Warp 8 is also the scheduler: lane 0 takes the next unit from the
+        // work counter one unit ahead (the atomic's latency hides behind the
+        // current unit's copies) and publishes it in the unit ring.
+        int taken = (kv_role == 0 && lane == 0) ? atomicAdd(a.sched, 1) : 0;
+        for (int it = 0;; ++it) {  // it: units started by this CTA
+            int unit;
+            if (kv_role == 0) {
+                unit = __shfl_sync(0xffffffffu, taken, 0);
+                const int s = it % kUnitRing;
+                if (it >= kUnitRing &&
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.unit_empty[s],
+                                                                (uint32_t)((it / kUnitRing - 1) & 1), LIM, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    sh.unit_ring[s] = unit;
+                    mbar_arrive(&sh.unit_full[s]);  // release: the index is visible to every waiter
+                    if (unit < total_units) taken = atomicAdd(a.sched, 1);
+                }
+            } else {
+                unit = read_unit(sh, it, LIM, abort_flag);
+                if (unit < 0) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (unit >= total_units) break;
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -303,13 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the first K tile does not depend on the Q buffer: issue it
                 // before waiting for the previous unit's last score MMA
                 ok = load_kv(0, 0);
-                if (ok && it > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty, (uint32_t)((it - 1) & 1), LIM, abort_flag)))
+                // Q stage it % 2; its previous use (unit it - 2) must have
+                // finished its last score MMA
+                const int qb = it & 1;
+                if (ok && it >= 2 &&
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[qb], (uint32_t)(((it - 2) >> 1) & 1), LIM,
+                                                                abort_flag)))
                     ok = false;
                 if (ok) {
-                    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full, TB);
+                    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qb], TB);
                     __syncwarp();
                     const int tok0 = u.cu0 + u.row0 / a.G;
-                    if (lane < Cfg::kHalves) tma_load_3d(sQ + lane * HB, &tm_q, &sh.q_full, lane * 64, u.g * a.G, tok0);
+                    if (lane < Cfg::kHalves)
+                        tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, u.g * a.G, tok0);
                 }
                 for (int j = 1; j < n && ok; ++j) ok = load_kv(j, 0);
             } else {
@@ -344,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rs = 0;                  // ring slot (K for warp 9, V for warp 11)
         uint32_t rph = 0;            // and the parity of its fill
         long long issued = 0;        // tiles issued by this warp
-        int ucnt = 0;                // units started
         bool ok = true;
         constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
@@ -359,7 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_lo0 = (uint32_t)smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
         const uint32_t tO = tmem + kTmemO;
         const bool s_role = (warp == kMmaWarp);
-        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++ucnt)) {
+        for (int ucnt = 0;; ++ucnt) {  // ucnt: units started
+            const int unit = read_unit(sh, ucnt, LIM, abort_flag);
+            if (unit < 0) {
+                ok = false;
+                break;
+            }
+            if (unit >= total_units) break;
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -368,11 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = tl.n_total;
             if (s_role) {
                 // S(j) = Q K(j)^T, as far ahead as the score buffers allow
-                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_full, (uint32_t)(ucnt & 1), LIM, abort_flag))) {
+                const int qb = ucnt & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&sh.q_full[qb], (uint32_t)((ucnt >> 1) & 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t q_lo_u = q_lo + (uint32_t)qb * (uint32_t)(TB >> 4);
                 for (int j = 0; j < n; ++j) {
                     if (issued >= kSBuf &&
                         !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.pv_done[ub], uph ^ 1u, LIM, abort_flag))) {
@@ -389,11 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
-                        umma_ss_warp2(d_tmem, q_lo + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                        umma_ss_warp2(d_tmem, q_lo_u + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
                     }
                     umma_commit_warp(&sh.s_full[ub]);
                     umma_commit_warp(&sh.k_empty[rs]);
-                    if (j == n - 1) umma_commit_warp(&sh.q_empty);  // Q is free once the last S is done
+                    if (j == n - 1) umma_commit_warp(&sh.q_empty[qb]);  // Q is free once the last S is done
                     ++issued;
                     if (++ub == kSBuf) {
                         ub = 0;
@@ -421,6 +482,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    int key0, valid;
+                    bool pooled;
+                    tl.tile(j, key0, valid, pooled);
+                    if (valid < kKT) {
+                        // keys past the tile's valid range: zero their V rows so
+                        // that P = 0 never meets a NaN or Inf left in the pool or
+                        // in this ring slot (16 bytes per lane; then a proxy fence,
+                        // as the MMA reads through the async proxy)
+                        uint8_t *vs_ = sV + rs * TB;
+                        const int per_half = (kKT - valid) * 8;  // 16-byte chunks per 64-column half
+                        for (int i = lane; i < per_half * Cfg::kHalves; i += 32) {
+                            const int h = i / per_half, rem = i - h * per_half;
+                            *reinterpret_cast<uint4 *>(vs_ + h * HB + (valid + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
                     const uint32_t v_lo = v_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
                     const uint32_t tP = tmem + ub * kKT;
 #pragma unroll
@@ -458,15 +537,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3) + 16 * (warp >> 2)) << 16);
         const uint32_t tO = lane_base + kTmemO;
         const float sl = a.scale_log2;
-        long long gt = 0;
         int cb = 0;          // score buffer of the next tile
         uint32_t cph = 0;    // and its use parity
         int prev_b = 0;      // buffer and use parity of the previous tile (for the PV(j-1) wait)
         uint32_t prev_ph = 0;
-        int oc = 0;
         bool ok = true;
-        int round = 0;
-        for (int unit = unit_of_round(0); unit < total_units; unit = unit_of_round(++round)) {
+        for (int oc = 0;; ++oc) {  // oc: units started
+            const int unit = read_unit(sh, oc, LIM, abort_flag);
+            if (unit < 0) {
+                ok = false;
+                break;
+            }
+            if (unit >= total_units) break;
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -476,6 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_valid = lr < u.rows;
             const int pos = row_valid ? u.C + (u.row0 + lr) / a.G : -1;
             float m_ref = -INFINITY, l = 0.f;
+            // a warp whose 16 rows are all padding (a decode has G rows of
+            // 128) skips the math; each O row depends on its own P row only,
+            // so whatever its P rows hold never reaches a written output
+            const bool warp_rows = __any_sync(0xffffffffu, row_valid);
             for (int j = 0; j < n; ++j) {
                 const int b = cb;
                 const uint32_t bph = cph;
@@ -486,6 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++cb == kSBuf) {
                     cb = 0;
                     cph ^= 1u;
+                }
+                if (!warp_rows) {
+                    mbar_arrive(&sh.p_full[b]);
+                    prev_b = b;
+                    prev_ph = bph;
+                    continue;
                 }
                 tc_fence_after();
                 const uint32_t tS = lane_base + b * kKT;
@@ -574,23 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st16x2_32<D / 2>(tO + c * 32, r);
                     }
                 }
-                if (valid < kKT) {
-                    // keys past the tile's valid range: zero their V rows so that
-                    // P = 0 never meets a NaN or Inf left in the pool or in smem
-                    const long long g = gt + j;
-                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[(int)(g % NSV)],
-                                                                    (uint32_t)((g / NSV) & 1), LIM, abort_flag))) {
-                        ok = false;
-                        break;
-                    }
-                    const int vr = tid >> 1, vh = tid & 1;  // V row, 64-column chunk
-                    if (vr >= valid && vh < Cfg::kHalves) {
-                        uint4 *q4 = reinterpret_cast<uint4 *>(sV + (int)(g % NSV) * TB + vh * HB + vr * 128);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) q4[i] = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.p_full[b]);
@@ -606,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = 1.f / l;
             const int t = u.cu0 + pr / a.G, h = u.g * a.G + pr % a.G;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / 64 && warp_rows; ++c) {
                 uint32_t r[32];
                 tmem_ld16x2_32<D / 2>(tO + c * 32, r);  // output columns half * D/2 + c * 32 + i
                 tmem_wait_ld();
@@ -635,7 +710,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&sh.o_empty);
-            ++oc;
             if (row_valid && half == 0) {
                 if (u.piece >= 0) {
                     float *ws = a.ws + u.ws_off;
@@ -645,7 +719,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.lse[(long long)t * a.hq + h] = (m_ref + __log2f(l)) * 0.69314718055994531f;
                 }
             }
-            gt += n;
         }
         if (!ok) {
             record_error(a.err, kErrTimeout);

@@ -112,6 +112,8 @@ struct Plan {
     int tile_m = 0;
     int tiles_per_unit = 1;
     int head_major = 0;
+    size_t sched_off = 0;   // byte offset of the work counter in the workspace
+    size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
     int direct_units = 0;
     int split_units = 0;
@@ -142,6 +144,12 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     // K/V of the batch larger than about half of L2: walk the direct units
     // head by head so that concurrent CTAs share K/V tiles in L2
     pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
+    pl.ws_bytes = (size_t)pl.ws_floats * sizeof(float);
+    if (tc) {
+        // the persistent kernel's work counter, after the partials
+        pl.sched_off = (pl.ws_bytes + 255) & ~(size_t)255;
+        pl.ws_bytes = pl.sched_off + 256;
+    }
     return pl;
 }
 
@@ -212,7 +220,7 @@ const char *cpa_status_string(cpa_status s) {
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params) {
     if (validate(batch, params) != CPA_SUCCESS || batch->num_reqs == 0) return 0;
     const Plan pl = make_plan(batch, params);
-    return (size_t)pl.ws_floats * sizeof(float);
+    return pl.ws_bytes;
 }
 
 cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, const void *k_new, const void *v_new,
@@ -253,7 +261,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return CPA_ERR_INVALID_ARG;
     const Plan pl = make_plan(batch, params);
-    const size_t need = (size_t)pl.ws_floats * sizeof(float);
+    const size_t need = pl.ws_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CPA_ERR_WORKSPACE;
     DeviceInfo dev;
     if (cpa_status s = device_info(dev)) return s;
@@ -300,7 +308,9 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     if (pl.tile_m == kTcTileM) {
         TcMaps maps;
         if (cpa_status s = make_tc_maps(batch, params, q, k_new, v_new, k_cache, v_cache, maps)) return s;
-        e = launch_attn_tc(a, maps, st);
+        a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
+        e = cudaMemsetAsync(a.sched, 0, sizeof(int), st);
+        if (e == cudaSuccess) e = launch_attn_tc(a, maps, st);
     } else {
         e = launch_attn_simt(a, params->dtype, st);
     }

@@ -103,6 +103,7 @@ struct AttnArgs {
     void *out;
     float *lse;
     float *ws;          // partials of split units
+    int *sched;         // tensor-core kernel: work counter (zeroed before the launch)
     int fuse_write;     // write new K/V into the pool in the prologue
     int write_ctas;     // CTAs that share the fused write
     int *err;           // device error word (first error wins)

@@ -121,10 +121,13 @@ typedef struct {
                                  0 = library default (2e9, about one second) */
 } cpa_params;
 
-/* Bytes of device workspace chunked_prefill_attention needs for this batch
- * (0 when no request is split).  Reads only host mirrors.  Returns 0 also
- * when the arguments are invalid; chunked_prefill_attention then reports
- * the error. */
+/* Bytes of device workspace chunked_prefill_attention needs for this batch:
+ * the split-KV partials of the requests that are split (rounded up to 256
+ * bytes) and, when the batch runs on the tensor-core kernel (BF16 with
+ * num_heads_q / num_heads_kv dividing 128), 256 bytes for that persistent
+ * kernel's work counter.  0 for an empty batch and for a CUDA-core batch
+ * with no split.  Reads only host mirrors.  Returns 0 also when the
+ * arguments are invalid; chunked_prefill_attention then reports the error. */
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params);
 
 /* Write the K/V rows of every active token into their pool slots: token i of
@@ -149,7 +152,9 @@ cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, cons
  * are only read.
  * workspace: device memory of at least chunked_prefill_workspace_size()
  * bytes (may be NULL when that size is 0); its contents need not be
- * initialised and are overwritten.  lse may be NULL. */
+ * initialised and are overwritten (the work counter by an asynchronous
+ * memset on `stream` before the launch), so two calls in flight at once
+ * need two workspaces.  lse may be NULL. */
 cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *params, const void *q,
                                      const void *k_new, const void *v_new, void *k_cache,
                                      void *v_cache, void *out, float *lse, void *workspace,

@@ -124,11 +124,16 @@ def test_workspace_size_counts_split_partials(lib):
     p = lib.Params(32, 8, 128, 16, 10000, 1024).c()
     b, keep = _cbatch(lib, [5000, 100, 2047], [1, 1, 1], 400)
     pieces = [-(-(5000 + 1) // 1024), 1, -(-(2047 + 1) // 1024)]
-    expect = sum(8 * n * 4 * (128 + 2) * 4 for n in pieces if n > 1)
+    partials = sum(8 * n * 4 * (128 + 2) * 4 for n in pieces if n > 1)
+    counter = 256  # the tensor-core kernel's work counter, after the partials
+    expect = -(-partials // 256) * 256 + counter
     assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == expect
-    # no split requested: no workspace
+    # no split requested: only the work counter
     p2 = lib.Params(32, 8, 128, 16, 10000, 1024, flags=lib.FLAG_NO_SPLIT).c()
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p2)) == 0
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p2)) == counter
     # a prefill chunk of 512 tokens spans many query tiles and is never split
     b3, keep3 = _cbatch(lib, [8000], [512], 600)
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b3), ctypes.byref(p)) == 0
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b3), ctypes.byref(p)) == counter
+    # the CUDA-core kernel (forced) keeps no counter
+    p4 = lib.Params(32, 8, 128, 16, 10000, 1024, flags=lib.FLAG_NO_SPLIT | lib.FLAG_FORCE_SIMT).c()
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b3), ctypes.byref(p4)) == 0
