@@ -242,8 +242,9 @@ def run_ours(args, rank, world, local):
     ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flops_step = sum(w.flops_per_step())
-    launches_per_step = len(w.steps) + sum(
-        1 for b in batches if cpa.workspace_size(b, params) > 0)  # attention (+ merge when split)
+    # attention, plus the merge kernel when some request is split: the workspace
+    # then holds partials in front of the 256-byte work counter
+    launches_per_step = len(w.steps) + sum(1 for b in batches if cpa.workspace_size(b, params) > 256)
 
     def one_step(evs=None):
         for i, (b, (q, k, v), o) in enumerate(zip(batches, inputs, outs)):
