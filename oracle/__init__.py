@@ -39,6 +39,8 @@ MUT_NO_BLOCK_TABLE = 5
 MUT_NO_SCALE = 6
 MUT_MERGE_NO_RESCALE = 7
 MUT_WRITE_OFF_BY_ONE = 8
+MUT_ROPE_INTERLEAVED = 9
+MUT_ROPE_NO_OFFSET = 10
 
 
 class _Problem(ctypes.Structure):
@@ -87,6 +89,9 @@ def _load():
         lib.cpa_oracle_attention.argtypes = [
             ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.cpa_oracle_rope.restype = ctypes.c_int
+        lib.cpa_oracle_rope.argtypes = [ctypes.POINTER(_Problem), ctypes.c_double, ctypes.c_void_p,
+                                        ctypes.c_void_p]
         lib.cpa_oracle_kv_write.restype = ctypes.c_int
         lib.cpa_oracle_kv_write.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int,
                                             ctypes.c_void_p, ctypes.c_void_p]
@@ -102,13 +107,16 @@ def default_threads() -> int:
 
 
 def _as_values(a: np.ndarray):
-    """Return (contiguous array, dtype code): float32 values or bfloat16 bits (uint16)."""
+    """Return (contiguous array, dtype code): float32 values, bfloat16 bits
+    (uint16) or float64 values."""
     a = np.ascontiguousarray(a)
     if a.dtype == np.float32:
         return a, 0
     if a.dtype == np.uint16:
         return a, 1
-    raise TypeError(f"oracle inputs must be float32 or bfloat16 bits (uint16), got {a.dtype}")
+    if a.dtype == np.float64:
+        return a, 2
+    raise TypeError(f"oracle inputs must be float32, float64 or bfloat16 bits (uint16), got {a.dtype}")
 
 
 class Batch:
@@ -216,3 +224,28 @@ def kv_write(batch: Batch, k_new, v_new, k_cache, v_cache, *, num_heads_kv, head
     if rc != 0:
         raise RuntimeError(f"oracle kv_write failed with status {rc}")
     return k_out, v_out
+
+
+def rope(batch: Batch, q, k_new, *, num_heads_q, num_heads_kv, head_dim, theta, mutation=MUT_NONE):
+    """Rotary position embedding (rotate-half form) of the active tokens'
+    queries [T, H_q, d] and new keys [T, H_kv, d] at absolute positions
+    cached_seq_len[r] + i, in fp64.  Returns (q_rot, k_rot) as float64."""
+    lib = _load()
+    T = batch.total_new_tokens
+    q = np.ascontiguousarray(q)
+    k_new = np.ascontiguousarray(k_new)
+    keep = []
+    v_dummy = np.zeros_like(k_new)
+    pool_dummy = np.zeros(num_heads_kv * head_dim, dtype=k_new.dtype)
+    P = _problem(batch, q, k_new, v_dummy, pool_dummy, pool_dummy, num_heads_q=num_heads_q,
+                 num_heads_kv=num_heads_kv, head_dim=head_dim, block_size=1, scale=1.0,
+                 mutation=mutation, keep=keep)
+    q_out = np.zeros((T, num_heads_q, head_dim), dtype=np.float64)
+    k_out = np.zeros((T, num_heads_kv, head_dim), dtype=np.float64)
+    if T == 0:
+        return q_out, k_out
+    rc = lib.cpa_oracle_rope(ctypes.byref(P), ctypes.c_double(float(theta)), q_out.ctypes.data,
+                             k_out.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle rope failed with status {rc}")
+    return q_out, k_out

@@ -34,6 +34,15 @@
  *    (the same values the write puts into the pool);
  *  - lse is the natural log of the softmax denominator of the scaled scores.
  *
+ * Rotary position embedding (optional, cpa_oracle_rope): "Prefill
+ * Optimisation", section 2, and "Chunked Prefill" note that the active
+ * tokens of a chunk take their absolute positions num_computed_tokens + i,
+ * which is where a rotary embedding must rotate them.  The pages fix no
+ * rotary convention; the reading taken is the rotate-half form of the
+ * RoFormer rotary embedding as used by Llama models: for a head vector x of
+ * dimension d at position p, each pair (x_c, x_{c+d/2}), c < d/2, turns by
+ * the angle p * theta^(-2c/d).
+ *
  * Parity pins (see tests/test_oracle.py): closed forms (first token of a
  * fresh prompt returns v_0; zero queries give the mean of visible values;
  * constant values; one-hot scores), a pure-Python fsum brute force over the
@@ -56,7 +65,7 @@ typedef struct {
     int32_t head_dim;
     int32_t block_size;
     int32_t num_blocks;
-    int32_t dtype;      /* 0: float32 values, 1: bfloat16 bit patterns (uint16) */
+    int32_t dtype;      /* 0: float32 values, 1: bfloat16 bit patterns (uint16), 2: float64 */
     int32_t mutation;   /* 0 in every real use; >0 plants a known mistake (tests only) */
     double scale;
     const int32_t *cached_seq_len;  /* [num_reqs] */
@@ -81,10 +90,13 @@ enum {
     MUT_NO_SCALE = 6,          /* scores not scaled */
     MUT_MERGE_NO_RESCALE = 7,  /* segment merge forgets to rescale l */
     MUT_WRITE_OFF_BY_ONE = 8,  /* KV write one slot too far */
+    MUT_ROPE_INTERLEAVED = 9,  /* rotary pairs (2c, 2c+1) instead of (c, c + d/2) */
+    MUT_ROPE_NO_OFFSET = 10,   /* rotary angle from i instead of cached_seq_len + i */
 };
 
 static double load_elem(const void *base, int dtype, size_t idx) {
     if (dtype == 0) return (double)((const float *)base)[idx];
+    if (dtype == 2) return ((const double *)base)[idx];
     uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -352,6 +364,43 @@ int cpa_oracle_kv_write(const orc_problem *P, int elem_bytes, void *k_cache, voi
             int t = P->cu_new_tokens[r] + i;
             memcpy((char *)k_cache + slot * row, (const char *)P->k_new + (size_t)t * row, row);
             memcpy((char *)v_cache + slot * row, (const char *)P->v_new + (size_t)t * row, row);
+        }
+    }
+    return 0;
+}
+
+/* Rotary position embedding of the active tokens' queries and new keys
+ * (see the header).  q_out [T, H_q, d] and k_out [T, H_kv, d] receive the
+ * rotated values in fp64 (either may be NULL).  Active token i of request r
+ * is at absolute position cached_seq_len[r] + i.  Returns 0 or -3. */
+int cpa_oracle_rope(const orc_problem *P, double theta, double *q_out, double *k_out) {
+    if (!P || !(theta > 0.0) || (P->head_dim & 1)) return -3;
+    const int d = P->head_dim, half = d / 2;
+    for (int t = 0; t < P->total_new_tokens; ++t) {
+        int r = request_of_token(P, t);
+        if (r < 0) return -3;
+        int i = t - P->cu_new_tokens[r];
+        double p = (P->mutation == MUT_ROPE_NO_OFFSET) ? (double)i : (double)(P->cached_seq_len[r] + i);
+        for (int which = 0; which < 2; ++which) {
+            const int heads = which == 0 ? P->num_heads_q : P->num_heads_kv;
+            const void *src = which == 0 ? P->q : P->k_new;
+            double *dst = which == 0 ? q_out : k_out;
+            if (!dst) continue;
+            for (int h = 0; h < heads; ++h) {
+                size_t base = ((size_t)t * heads + h) * d;
+                for (int c = 0; c < half; ++c) {
+                    /* pair members: (c, c + d/2); the planted mistake pairs (2c, 2c+1) */
+                    int a = c, b = c + half;
+                    if (P->mutation == MUT_ROPE_INTERLEAVED) {
+                        a = 2 * c;
+                        b = 2 * c + 1;
+                    }
+                    double angle = p * pow(theta, -2.0 * c / d);
+                    double x0 = load_elem(src, P->dtype, base + a), x1 = load_elem(src, P->dtype, base + b);
+                    dst[base + a] = x0 * cos(angle) - x1 * sin(angle);
+                    dst[base + b] = x1 * cos(angle) + x0 * sin(angle);
+                }
+            }
         }
     }
     return 0;
