@@ -18,6 +18,7 @@ and a secondary line for the decode-heavy mixed step (KV-read GB/s).
 --case times one attention call of a single workload step (for profiling
 under ncu and per-configuration timing) and prints {"case": ..., "ms": ...}:
   llama_chunk        last 1808-token chunk of the Llama-3-8B prompt (bs 128)
+  llama_chunk_rope   the same with the rotary embedding applied in the call (theta 5e5)
   long_context_last  last 2048-token chunk of the 32,768-token prompt
                      (H_q 64, bs 16, cached 30,720)
   mixed_step         64 decodes + 512-token chunks under a 2048 budget
@@ -49,12 +50,13 @@ METRIC = "chunk-attn TFLOP/s (algorithmic, visible pairs only)"
 UNIT = "TFLOP/s"
 
 
-# name -> (workload constructor, step index)
+# name -> (workload constructor, step index, rope_theta)
 CASES = {
-    "llama_chunk": (W.llama3_8b_prompt, -1),
-    "long_context_last": (W.long_context, -1),
-    "mixed_step": (W.mixed_step, 0),
-    "prefix_cache": (W.prefix_cache, 0),
+    "llama_chunk": (W.llama3_8b_prompt, -1, 0.0),
+    "llama_chunk_rope": (W.llama3_8b_prompt, -1, 500000.0),
+    "long_context_last": (W.long_context, -1, 0.0),
+    "mixed_step": (W.mixed_step, 0, 0.0),
+    "prefix_cache": (W.prefix_cache, 0, 0.0),
 }
 
 
@@ -394,14 +396,14 @@ def run_case(args, local):
     cpa.load()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    make, idx = CASES[args.case]
+    make, idx, rope_theta = CASES[args.case]
     w = make()
     sh = w.shape
     t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
     s = w.steps[idx]
     params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
                         sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16 if sh.dtype == "bf16" else cpa.DTYPE_FP32,
-                        cpa.FLAG_FUSE_KV_WRITE)
+                        cpa.FLAG_FUSE_KV_WRITE, rope_theta=rope_theta)
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
     q, k, v = t.step_inputs(s)
     out = torch.empty_like(q)

@@ -67,6 +67,7 @@ class _Params(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
         ("timeout_cycles", ctypes.c_int64),
+        ("rope_theta", ctypes.c_float),
     ]
 
 
@@ -129,11 +130,13 @@ class Params:
     dtype: int = DTYPE_BF16
     flags: int = FLAG_FUSE_KV_WRITE
     timeout_cycles: int = 0
+    rope_theta: float = 0.0
 
     def c(self) -> _Params:
         scale = self.scale if self.scale is not None else 1.0 / float(np.sqrt(self.head_dim))
         return _Params(self.num_heads_q, self.num_heads_kv, self.head_dim, self.block_size, self.num_blocks,
-                       self.kv_segment_size, scale, self.dtype, self.flags, self.timeout_cycles)
+                       self.kv_segment_size, scale, self.dtype, self.flags, self.timeout_cycles,
+                       self.rope_theta)
 
 
 class Batch:

@@ -82,6 +82,7 @@ cpa_status validate(const cpa_batch *b, const cpa_params *p) {
     if (ks != 0 && ks != 512 && ks != 1024 && ks != 2048 && ks != 4096) return CPA_ERR_INVALID_ARG;
     if (ks != 0 && ks % p->block_size != 0) return CPA_ERR_INVALID_ARG;
     if (!isfinite(p->scale) || !(p->scale > 0.f)) return CPA_ERR_INVALID_ARG;
+    if (!isfinite(p->rope_theta) || p->rope_theta < 0.f) return CPA_ERR_INVALID_ARG;
     if (p->timeout_cycles < 0) return CPA_ERR_INVALID_ARG;
     if (b->num_reqs < 0 || b->total_new_tokens < 0) return CPA_ERR_INVALID_ARG;
     if (b->num_reqs == 0) return b->total_new_tokens == 0 ? CPA_SUCCESS : CPA_ERR_INVALID_ARG;
@@ -113,6 +114,7 @@ struct Plan {
     int tiles_per_unit = 1;
     int head_major = 0;
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
+    size_t rq_off = 0, rk_off = 0;  // rotated q / k_new copies (rope_theta > 0)
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
     int direct_units = 0;
@@ -145,6 +147,13 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     // head by head so that concurrent CTAs share K/V tiles in L2
     pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
     pl.ws_bytes = (size_t)pl.ws_floats * sizeof(float);
+    if (p->rope_theta > 0.f) {
+        // rotated copies of q and k_new, which the attention then reads
+        const size_t T = (size_t)b->total_new_tokens, es = (size_t)elem_bytes(p), d = (size_t)p->head_dim;
+        pl.rq_off = (pl.ws_bytes + 255) & ~(size_t)255;
+        pl.rk_off = (pl.rq_off + T * p->num_heads_q * d * es + 255) & ~(size_t)255;
+        pl.ws_bytes = pl.rk_off + T * p->num_heads_kv * d * es;
+    }
     if (tc) {
         // the persistent kernel's work counter, after the partials
         pl.sched_off = (pl.ws_bytes + 255) & ~(size_t)255;
@@ -195,6 +204,28 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
     return CPA_SUCCESS;
 }
 
+RopeArgs rope_args(const cpa_batch *batch, const cpa_params *params, int *err) {
+    RopeArgs r{};
+    r.num_reqs = batch->num_reqs;
+    r.max_blocks = batch->max_blocks_per_seq;
+    r.total_tokens = batch->total_new_tokens;
+    r.cached = batch->cached_seq_len;
+    r.cu = batch->cu_new_tokens;
+    r.bt = batch->block_table;
+    r.hq = params->num_heads_q;
+    r.hkv = params->num_heads_kv;
+    r.d = params->head_dim;
+    r.bs = params->block_size;
+    r.num_blocks = params->num_blocks;
+    r.elem_bytes = elem_bytes(params);
+    for (int c = 0; c < params->head_dim / 2; ++c) {
+        const double turns = pow((double)params->rope_theta, -2.0 * c / params->head_dim) / 6.283185307179586477;
+        r.turn_frac[c] = (unsigned long long)ldexp(turns, 64);  // turns < 1 / (2 pi): fits
+    }
+    r.err = err;
+    return r;
+}
+
 }  // namespace
 }  // namespace cpa
 
@@ -232,6 +263,16 @@ cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, cons
         return CPA_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (cpa_status s = device_info(dev)) return s;
+    if (params->rope_theta > 0.f) {
+        // rotated keys and the values go to the pool; no rotated copies are kept
+        RopeArgs r = rope_args(batch, params, dev.err);
+        r.k_new = k_new;
+        r.v_new = v_new;
+        r.write_pool = 1;
+        r.k_cache = k_cache;
+        r.v_cache = v_cache;
+        return launch_rope(r, dev.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CPA_SUCCESS : CPA_ERR_CUDA;
+    }
     KvWriteArgs a{};
     a.num_reqs = batch->num_reqs;
     a.max_blocks = batch->max_blocks_per_seq;
@@ -266,6 +307,24 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     DeviceInfo dev;
     if (cpa_status s = device_info(dev)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
+    if (params->rope_theta > 0.f) {
+        // rotate q and k_new into the workspace (and, for a fused write, put the
+        // rotated keys and the values into the pool); the attention reads the copies
+        RopeArgs r = rope_args(batch, params, dev.err);
+        r.q = q;
+        r.k_new = k_new;
+        r.v_new = v_new;
+        r.q_rot = static_cast<char *>(workspace) + pl.rq_off;
+        r.k_rot = static_cast<char *>(workspace) + pl.rk_off;
+        r.write_pool = fuse_write ? 1 : 0;
+        r.k_cache = k_cache;
+        r.v_cache = v_cache;
+        if (launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
+        q = r.q_rot;
+        k_new = r.k_rot;
+        fuse_write = false;
+    }
 
     AttnArgs a{};
     a.num_reqs = batch->num_reqs;
@@ -296,7 +355,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.out = out;
     a.lse = lse;
     a.ws = static_cast<float *>(workspace);
-    a.fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) ? 1 : 0;
+    a.fuse_write = fuse_write ? 1 : 0;
     const int units = pl.direct_units + pl.split_units;
     // the tensor-core kernel is persistent: at most one CTA per SM
     a.write_ctas = (pl.tile_m == kTcTileM) ? (units < dev.sms ? units : dev.sms) : units;

@@ -111,6 +111,31 @@ struct AttnArgs {
     int test_stall;     // testing only: withhold the first K tile's copies
 };
 
+// Arguments of the rotary pre-pass: rotates the active tokens' queries and
+// new keys at absolute position cached[r] + i (pairs (c, c + d/2) turned by
+// p * theta^(-2c/d)) into q_rot / k_rot, and with write_pool also stores the
+// rotated keys and the values into their pool slots.
+struct RopeArgs {
+    int num_reqs, max_blocks, total_tokens;
+    const int32_t *cached;
+    const int32_t *cu;
+    const int32_t *bt;
+    int hq, hkv, d, bs, num_blocks;
+    int elem_bytes;       // 2 (bf16) or 4 (fp32)
+    // turns per position of pair c, theta^(-2c/d) / (2 pi), as a 64-bit binary
+    // fraction: pos * turn_frac[c] modulo 2^64 is the angle reduced to one turn
+    unsigned long long turn_frac[64];
+    const void *q;        // [T, hq, d] (may be null when q_rot is null)
+    const void *k_new;    // [T, hkv, d]
+    const void *v_new;    // [T, hkv, d]
+    void *q_rot;          // [T, hq, d] or null
+    void *k_rot;          // [T, hkv, d] or null
+    int write_pool;
+    void *k_cache;
+    void *v_cache;
+    int *err;
+};
+
 // Arguments of the standalone KV write.
 struct KvWriteArgs {
     int num_reqs, max_blocks, total_tokens;

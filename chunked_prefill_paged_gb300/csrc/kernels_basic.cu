@@ -37,6 +37,108 @@ cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stre
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ rotary pre-pass
+// One warp per (active token, group of kHeadsPerWarp heads; query heads first,
+// then key heads).  The angle of pair c is reduced to one turn exactly in
+// integer arithmetic: turn_frac[c] holds theta^(-2c/d) / (2 pi) as a 64-bit
+// binary fraction, so pos * turn_frac[c] modulo 2^64 (a wrapping 64-bit
+// product) is the fraction of a turn; its top 24 bits give the angle in
+// [0, 2 pi), whose cosine and sine are taken in fp32.  The rotation runs in
+// fp32 and is rounded to the element type.  Lane l owns pairs c = 2l, 2l + 1
+// (d = 128) or c = l (d = 64), so the warp's accesses to each half row are
+// contiguous.
+constexpr int kHeadsPerWarp = 8;
+
+// PPL consecutive elements of a lane moved as one access
+template <int BYTES> struct LaneVec;
+template <> struct LaneVec<2> { using type = unsigned short; };
+template <> struct LaneVec<4> { using type = unsigned int; };
+template <> struct LaneVec<8> { using type = uint2; };
+
+template <int D, typename T>
+__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
+    constexpr int PPL = D / 64;   // pairs per lane
+    constexpr int HALF = D / 2;
+    __shared__ unsigned long long frac_s[HALF];
+    for (int c = threadIdx.x; c < HALF; c += blockDim.x) frac_s[c] = a.turn_frac[c];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int heads = a.hq + a.hkv;
+    const int groups = (heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const long long wid = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (wid >= (long long)a.total_tokens * groups) return;
+    const int t = (int)(wid / groups), grp = (int)(wid % groups);
+    const int r = request_of_token(a.cu, a.num_reqs, t);
+    const int pos = __ldg(a.cached + r) + (t - __ldg(a.cu + r));
+    float cs[PPL], sn[PPL];
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) {
+        const unsigned long long turn = (unsigned long long)pos * frac_s[lane * PPL + e];  // wraps: mod 1 turn
+        const float ang = (float)(turn >> 40) * (6.28318530717958648f / 16777216.0f);
+        sincosf(ang, &sn[e], &cs[e]);
+    }
+    long long slot = -1;
+    if (a.write_pool) slot = slot_of(a.bt, a.max_blocks, a.bs, a.num_blocks, r, pos, a.err);
+    const int h_end = min(heads, (grp + 1) * kHeadsPerWarp);
+    for (int head = grp * kHeadsPerWarp; head < h_end; ++head) {
+        const bool is_q = head < a.hq;
+        if (is_q && a.q_rot == nullptr) continue;
+        const int hh = is_q ? head : head - a.hq;
+        const long long row = ((long long)t * (is_q ? a.hq : a.hkv) + hh) * D;
+        using V = typename LaneVec<PPL * (int)sizeof(T)>::type;
+        const T *src = static_cast<const T *>(is_q ? a.q : a.k_new) + row + lane * PPL;
+        union {
+            V v;
+            T e[PPL];
+        } xl, xh;
+        xl.v = *reinterpret_cast<const V *>(src);
+        xh.v = *reinterpret_cast<const V *>(src + HALF);
+#pragma unroll
+        for (int e = 0; e < PPL; ++e) {
+            const float x0 = to_float(xl.e[e]), x1 = to_float(xh.e[e]);
+            xl.e[e] = from_float<T>(x0 * cs[e] - x1 * sn[e]);
+            xh.e[e] = from_float<T>(x1 * cs[e] + x0 * sn[e]);
+        }
+        T *dst = nullptr;
+        if (is_q) dst = static_cast<T *>(a.q_rot) + row;
+        else if (a.k_rot) dst = static_cast<T *>(a.k_rot) + row;
+        T *kp = (!is_q && slot >= 0) ? static_cast<T *>(a.k_cache) + (slot * a.hkv + hh) * D : nullptr;
+        if (dst) {
+            *reinterpret_cast<V *>(dst + lane * PPL) = xl.v;
+            *reinterpret_cast<V *>(dst + HALF + lane * PPL) = xh.v;
+        }
+        if (kp) {
+            *reinterpret_cast<V *>(kp + lane * PPL) = xl.v;
+            *reinterpret_cast<V *>(kp + HALF + lane * PPL) = xh.v;
+        }
+        if (kp) {  // the value row goes to the same slot unchanged, 16 bytes per lane
+            const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + row);
+            uint4 *vp = reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + (slot * a.hkv + hh) * D);
+            for (int c = lane; c < D * (int)sizeof(T) / 16; c += 32) vp[c] = vs[c];
+        }
+    }
+}
+
+cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream) {
+    (void)num_sms;
+    if (a.total_tokens == 0) return cudaSuccess;
+    const int warps = 8;
+    const long long work = (long long)a.total_tokens * ((a.hq + a.hkv + kHeadsPerWarp - 1) / kHeadsPerWarp);
+    const int blocks = (int)((work + warps - 1) / warps);
+    if (a.elem_bytes == 2) {
+        if (a.d == 128)
+            rope_kernel<128, __nv_bfloat16><<<blocks, warps * 32, 0, stream>>>(a);
+        else
+            rope_kernel<64, __nv_bfloat16><<<blocks, warps * 32, 0, stream>>>(a);
+    } else {
+        if (a.d == 128)
+            rope_kernel<128, float><<<blocks, warps * 32, 0, stream>>>(a);
+        else
+            rope_kernel<64, float><<<blocks, warps * 32, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------- CUDA-core attention
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll

@@ -19,6 +19,7 @@ struct TcMaps {
 };
 
 cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t stream);
 cudaError_t launch_attn_merge(const AttnArgs &a, int dtype, int num_split_reqs, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs &a, const TcMaps &maps, cudaStream_t stream);

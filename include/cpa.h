@@ -119,6 +119,15 @@ typedef struct {
     uint32_t flags;           /* CPA_FLAG_* */
     int64_t timeout_cycles;   /* bound of every device-side wait, in SM clock cycles;
                                  0 = library default (2e9, about one second) */
+    float rope_theta;         /* 0: q and k_new are used as given (already position-encoded).
+                                 > 0: rotary position embedding with this base is applied first:
+                                 query and new key of active token i of request r are rotated at
+                                 absolute position cached_seq_len[r] + i ("Prefill Optimisation",
+                                 section 2: chunk tokens keep their absolute positions), each pair
+                                 (x_c, x_{c+d/2}) turned by p * rope_theta^(-2c/d) (rotate-half
+                                 form), in fp32 and rounded to the element type.  The rotated keys
+                                 are what the K/V write stores.  The caller's q and k_new are not
+                                 modified: the rotated copies live in the workspace. */
 } cpa_params;
 
 /* Bytes of device workspace chunked_prefill_attention needs for this batch:

@@ -64,6 +64,8 @@ BAD_PARAMS = [
     dict(dtype=5),
     dict(scale=float("inf")),
     dict(scale=-0.1),
+    dict(rope_theta=-1.0),
+    dict(rope_theta=float("nan")),
 ]
 
 
@@ -137,3 +139,14 @@ def test_workspace_size_counts_split_partials(lib):
     # the CUDA-core kernel (forced) keeps no counter
     p4 = lib.Params(32, 8, 128, 16, 10000, 1024, flags=lib.FLAG_NO_SPLIT | lib.FLAG_FORCE_SIMT).c()
     assert L.chunked_prefill_workspace_size(ctypes.byref(b3), ctypes.byref(p4)) == 0
+
+
+def test_workspace_size_counts_rotated_copies(lib):
+    L = lib.load()
+    b, keep = _cbatch(lib, [8000], [512], 600)
+    plain = L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(lib.Params(32, 8, 128, 16, 10000, 1024).c()))
+    p = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0).c()
+    rq = 512 * 32 * 128 * 2   # rotated queries, bf16
+    rk = 512 * 8 * 128 * 2    # rotated new keys
+    # the copies come first (256-byte aligned), the work counter stays last
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + rk + plain
