@@ -23,6 +23,7 @@ under ncu and per-configuration timing) and prints {"case": ..., "ms": ...}:
                      (H_q 64, bs 16, cached 30,720)
   mixed_step         64 decodes + 512-token chunks under a 2048 budget
   prefix_cache       16 requests sharing a 4096-token cached prefix
+  speculative_decode 64 requests x 5 tokens (1 + 4 drafts) over contexts U{1024..32768}
 """
 from __future__ import annotations
 
@@ -57,6 +58,7 @@ CASES = {
     "long_context_last": (W.long_context, -1, 0.0),
     "mixed_step": (W.mixed_step, 0, 0.0),
     "prefix_cache": (W.prefix_cache, 0, 0.0),
+    "speculative_decode": (W.speculative_decode, 0, 0.0),
 }
 
 

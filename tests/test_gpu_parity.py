@@ -187,6 +187,13 @@ def test_config_mixed_step(cpa):
     assert_within(res, "bf16")
 
 
+def test_speculative_decode_queries(cpa):
+    # short causal chunks (1 + 4 draft tokens) over long contexts, split into
+    # kv_segment_size pieces and merged
+    res = run_and_compare(W.speculative_decode(num_reqs=16), rows_per_req=2)
+    assert_within(res, "bf16")
+
+
 def test_config_long_context(cpa):
     res = run_and_compare(W.long_context(), rows_per_req=6, steps_to_check=[0, 7, 15])
     assert_within(res, "bf16")

@@ -376,6 +376,19 @@ def mixed_step(seed: int = 1004, num_decodes: int = 64, budget: int = 2048, chun
     return w
 
 
+def speculative_decode(seed: int = 1006, num_reqs: int = 64, drafts: int = 4) -> Workload:
+    """Decodes that verify draft tokens: each request brings 1 + drafts active
+    tokens ("Prefill Processing", Attention Metadata: decode_token_threshold =
+    1 + max_num_draft_tokens) over a context uniform{1024..32768}; H 32/8,
+    d 128, block 16, kv_segment_size 1024, pool = needed + 10%."""
+    sh = Shape(32, 8, 128, 16, 1024, "bf16")
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(1024, 32769, size=num_reqs)
+    reqs = [(int(c), 1 + drafts) for c in ctx]
+    return make_batch_workload(f"speculative_decode_{num_reqs}x{1 + drafts}", sh, reqs, seed, spare=0.1,
+                               description=f"{num_reqs} requests x {1 + drafts} tokens over C~U{{1024..32768}}; bs 16")
+
+
 def long_context(seed: int = 1005) -> Workload:
     """70B-shaped GQA: a 32,768-token prompt in 16 chunks of 2048 (last step
     cached 30,720), H_q 64, H_kv 8, d 128, block 16, kv_segment_size 4096,
@@ -391,4 +404,5 @@ ALL = {
     "prefix_cache": prefix_cache,
     "mixed_step": mixed_step,
     "long_context": long_context,
+    "speculative_decode": speculative_decode,
 }
