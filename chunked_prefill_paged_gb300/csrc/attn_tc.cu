@@ -20,7 +20,10 @@
 //              its threads 0-15 the row's keys 0-63 (output columns 0 .. D/2-1)
 //              and threads 16-31 keys 64-127 (columns D/2 .. D-1); the row
 //              maximum and sum are combined with one shuffle.  They also do
-//              this CTA's share of the fused K/V write first.
+//              the fused K/V write: its pieces follow the attention units in
+//              the work counter, so CTAs whose attention work has run out take
+//              them (this kernel reads new keys from k_new / v_new, so the
+//              pool rows are only needed by the next call).
 //   warp 8     TMA producer of Q per unit and of the K tiles; warp 10 of the V
 //              tiles, each into its own ring, so a V slot still in use never
 //              holds up the next K copy.  A pool tile is one box per cache
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
     const long long LIM = a.timeout_cycles;
     const int total_units = a.num_direct_units + a.num_split_units;
+    const int end_index = total_units + a.write_chunks;  // then the fused K/V write
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -267,8 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;      // parity of that slot's current fill
         int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
         // Warp 8 is also the scheduler: lane 0 takes the next unit from the
-        // work counter one unit ahead (the atomic's latency hides behind the
-        // current unit's copies) and publishes it in the unit ring.
+        // work counter once it has issued the current unit's last K copies,
+        // a few tiles before the CTA runs out of work (claimed any earlier,
+        // the last units would wait behind busy CTAs while others idle), and
+        // publishes it to the other roles through the unit ring.
         int taken = (kv_role == 0 && lane == 0) ? atomicAdd(a.sched, 1) : 0;
         for (int it = 0;; ++it) {  // it: units started by this CTA
             int unit;
@@ -284,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     sh.unit_ring[s] = unit;
                     mbar_arrive(&sh.unit_full[s]);  // release: the index is visible to every waiter
-                    if (unit < total_units) taken = atomicAdd(a.sched, 1);
+                    // pieces of the K/V write need no copies: claim the next index now
+                    if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
                 }
             } else {
                 unit = read_unit(sh, it, LIM, abort_flag);
@@ -293,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
-            if (unit >= total_units) break;
+            if (unit >= end_index) break;
+            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -365,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, u.g * a.G, tok0);
                 }
                 for (int j = 1; j < n && ok; ++j) ok = load_kv(j, 0);
+                if (lane == 0) taken = atomicAdd(a.sched, 1);  // this unit's copies are all issued
             } else {
                 for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 1);
             }
@@ -417,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            if (unit >= total_units) break;
+            if (unit >= end_index) break;
+            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);
@@ -533,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================== softmax (warps 0-7)
         const int half = lane >> 4;                                // 0: keys 0-63, 1: keys 64-127
         const int lr = 32 * (warp & 3) + 16 * (warp >> 2) + (lane & 15);  // row of the tile == TMEM lane
-        if (a.fuse_write) fused_write_share(a, blockIdx.x, gridDim.x, tid, kSoftmaxThreads, 2);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3) + 16 * (warp >> 2)) << 16);
         const uint32_t tO = lane_base + kTmemO;
         const float sl = a.scale_log2;
@@ -548,7 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            if (unit >= total_units) break;
+            if (unit >= end_index) break;
+            if (unit >= total_units) {
+                // a piece of the fused K/V write.  This kernel reads new keys
+                // from k_new / v_new, so the pool rows are only for the next
+                // call; CTAs take these pieces once attention work runs out.
+                const long long total = (long long)a.total_tokens * a.hkv * (D * 2 / 16);
+                const long long b = (long long)(unit - total_units) * kWriteChunkPieces;
+                const long long e = b + kWriteChunkPieces < total ? b + kWriteChunkPieces : total;
+                scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, D * 2,
+                               a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, kSoftmaxThreads, a.err);
+                continue;
+            }
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             Unit u;
             decode_unit(a, unit, u);

@@ -356,9 +356,16 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.lse = lse;
     a.ws = static_cast<float *>(workspace);
     a.fuse_write = fuse_write ? 1 : 0;
+    if (pl.tile_m == kTcTileM && fuse_write) {
+        const long long pieces = (long long)batch->total_new_tokens * params->num_heads_kv *
+                                 (params->head_dim * elem_bytes(params) / 16);
+        a.write_chunks = (int)((pieces + kWriteChunkPieces - 1) / kWriteChunkPieces);
+    }
     const int units = pl.direct_units + pl.split_units;
-    // the tensor-core kernel is persistent: at most one CTA per SM
-    a.write_ctas = (pl.tile_m == kTcTileM) ? (units < dev.sms ? units : dev.sms) : units;
+    // the tensor-core kernel is persistent: at most one CTA per SM, and no
+    // more than it has attention units and write pieces
+    const int work = units + a.write_chunks;
+    a.write_ctas = (pl.tile_m == kTcTileM) ? (work < dev.sms ? work : dev.sms) : units;
     a.err = dev.err;
     a.timeout_cycles = params->timeout_cycles > 0 ? params->timeout_cycles : kDefaultTimeoutCycles;
     a.test_stall = (params->flags & CPA_FLAG_TEST_STALL) ? 1 : 0;

@@ -32,6 +32,9 @@ constexpr int kTcTileM = 128;    // packed query rows per tensor-core tile
 constexpr int kTcTileN = 128;    // keys per K/V tile of the tensor-core kernel
 constexpr int kSimtTileM = 16;   // packed query rows per CUDA-core tile
 constexpr int kDefaultSplit = 1024;
+// 16-byte pieces of the new K/V rows per fused-write chunk of the tensor-core
+// kernel (each piece index copies 16 bytes of K and 16 bytes of V)
+constexpr int kWriteChunkPieces = 1024;
 // Batches whose K/V (all requests, cached + new) exceed this many bytes walk
 // their direct units kv head by kv head (about half of GB300's L2).
 constexpr double kHeadMajorKvBytes = 64.0 * 1024 * 1024;
@@ -104,6 +107,9 @@ struct AttnArgs {
     float *lse;
     float *ws;          // partials of split units
     int *sched;         // tensor-core kernel: work counter (zeroed before the launch)
+    int write_chunks;   // tensor-core kernel with the fused write: indices [units, units +
+                        // write_chunks) of the counter are pieces of the K/V write, taken
+                        // by CTAs whose attention work has run out
     int fuse_write;     // write new K/V into the pool in the prologue
     int write_ctas;     // CTAs that share the fused write
     int *err;           // device error word (first error wins)
