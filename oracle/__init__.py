@@ -41,6 +41,9 @@ MUT_MERGE_NO_RESCALE = 7
 MUT_WRITE_OFF_BY_ONE = 8
 MUT_ROPE_INTERLEAVED = 9
 MUT_ROPE_NO_OFFSET = 10
+MUT_FP8_NEW_UNQUANTIZED = 11
+MUT_FP8_HEAD0_SCALE = 12
+MUT_FP8_TRUNCATE = 13
 
 
 class _Problem(ctypes.Structure):
@@ -65,6 +68,9 @@ class _Problem(ctypes.Structure):
         ("v_new", ctypes.c_void_p),
         ("k_cache", ctypes.c_void_p),
         ("v_cache", ctypes.c_void_p),
+        ("kv_fp8", ctypes.c_int32),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -89,6 +95,12 @@ def _load():
         lib.cpa_oracle_attention.argtypes = [
             ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.cpa_oracle_kv_write_fp8.restype = ctypes.c_int
+        lib.cpa_oracle_kv_write_fp8.argtypes = [ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_void_p]
+        lib.cpa_oracle_e4m3_encode.restype = None
+        lib.cpa_oracle_e4m3_encode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_long, ctypes.c_int]
+        lib.cpa_oracle_e4m3_decode.restype = None
+        lib.cpa_oracle_e4m3_decode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_long]
         lib.cpa_oracle_rope.restype = ctypes.c_int
         lib.cpa_oracle_rope.argtypes = [ctypes.POINTER(_Problem), ctypes.c_double, ctypes.c_void_p,
                                         ctypes.c_void_p]
@@ -143,12 +155,28 @@ class Batch:
 
 
 def _problem(batch: Batch, q, k_new, v_new, k_cache, v_cache, *, num_heads_q, num_heads_kv,
-             head_dim, block_size, scale, mutation, keep):
+             head_dim, block_size, scale, mutation, keep, kv_scales=None):
     q, dt = _as_values(q)
     k_new, dt1 = _as_values(k_new)
     v_new, dt2 = _as_values(v_new)
-    k_cache, dt3 = _as_values(k_cache)
-    v_cache, dt4 = _as_values(v_cache)
+    if kv_scales is None:
+        k_cache, dt3 = _as_values(k_cache)
+        v_cache, dt4 = _as_values(v_cache)
+    else:
+        # FP8 pools: E4M3 codes, one byte per element
+        k_cache = np.ascontiguousarray(k_cache)
+        v_cache = np.ascontiguousarray(v_cache)
+        if k_cache.dtype != np.uint8 or v_cache.dtype != np.uint8:
+            raise TypeError("FP8 pools must be uint8 arrays of E4M3 codes")
+        dt3 = dt4 = dt
+        k_scale = np.ascontiguousarray(np.asarray(kv_scales[0], dtype=np.float32))
+        v_scale = np.ascontiguousarray(np.asarray(kv_scales[1], dtype=np.float32))
+        if k_scale.shape != (num_heads_kv,) or v_scale.shape != (num_heads_kv,):
+            raise ValueError("k_scale / v_scale must hold one scale per kv head")
+        if not (np.all(np.isfinite(k_scale)) and np.all(k_scale > 0) and np.all(np.isfinite(v_scale))
+                and np.all(v_scale > 0)):
+            raise ValueError("FP8 scales must be finite and > 0")
+        keep.extend([k_scale, v_scale])
     if len({dt, dt1, dt2, dt3, dt4}) != 1:
         raise TypeError("q, k_new, v_new and the pools must share one element type")
     T = batch.total_new_tokens
@@ -163,12 +191,16 @@ def _problem(batch: Batch, q, k_new, v_new, k_cache, v_cache, *, num_heads_q, nu
         batch.cu_new_tokens.ctypes.data, batch.block_table.ctypes.data,
         q.ctypes.data, k_new.ctypes.data, v_new.ctypes.data, k_cache.ctypes.data,
         v_cache.ctypes.data)
+    if kv_scales is not None:
+        P.kv_fp8 = 1
+        P.k_scale = k_scale.ctypes.data
+        P.v_scale = v_scale.ctypes.data
     return P
 
 
 def attention(batch: Batch, q, k_new, v_new, k_cache, v_cache, *, num_heads_q, num_heads_kv,
               head_dim, block_size, scale, rows=None, segmented=False, kv_segment_size=0,
-              threads=None, mutation=MUT_NONE):
+              threads=None, mutation=MUT_NONE, k_scale=None, v_scale=None):
     """fp64 attention output [n_rows, H_q, d] and lse [n_rows, H_q] (natural log).
 
     rows: token indices into the packed batch (None = all tokens).  With
@@ -177,12 +209,18 @@ def attention(batch: Batch, q, k_new, v_new, k_cache, v_cache, *, num_heads_q, n
     evaluated directly.  Inputs: float32 arrays or bfloat16 bit patterns
     (uint16) of q [T,H_q,d], k_new/v_new [T,H_kv,d], pools
     [num_blocks, block_size, H_kv, d].
+
+    FP8 cache: with k_scale / v_scale ([H_kv] each) the pools are uint8 E4M3
+    codes; a code c of kv head g stands for value(c) * scale[g], and the
+    active tokens' own K/V rows are taken through the same encoding (as the
+    cache holds them).
     """
     lib = _load()
     keep = []
+    fp8 = _fp8_scales(k_scale, v_scale)
     P = _problem(batch, q, k_new, v_new, k_cache, v_cache, num_heads_q=num_heads_q,
                  num_heads_kv=num_heads_kv, head_dim=head_dim, block_size=block_size, scale=scale,
-                 mutation=mutation, keep=keep)
+                 mutation=mutation, keep=keep, kv_scales=fp8)
     if rows is None:
         n_rows = batch.total_new_tokens
         rows_arr = None
@@ -203,15 +241,34 @@ def attention(batch: Batch, q, k_new, v_new, k_cache, v_cache, *, num_heads_q, n
     return out, lse
 
 
+def _fp8_scales(k_scale, v_scale):
+    if (k_scale is None) != (v_scale is None):
+        raise ValueError("give both k_scale and v_scale, or neither")
+    return None if k_scale is None else (k_scale, v_scale)
+
+
 def kv_write(batch: Batch, k_new, v_new, k_cache, v_cache, *, num_heads_kv, head_dim, block_size,
-             mutation=MUT_NONE):
+             mutation=MUT_NONE, k_scale=None, v_scale=None):
     """Return copies of the pools with every active token's K/V row written
-    into its slot (block_table[r][(C+i)//bs]*bs + (C+i)%bs).  A byte copy."""
+    into its slot (block_table[r][(C+i)//bs]*bs + (C+i)%bs).  A byte copy;
+    with k_scale / v_scale the pools are uint8 E4M3 codes and each element is
+    encoded with its kv head's scale (see e4m3_encode)."""
     lib = _load()
     k_out = np.array(k_cache, copy=True, order="C")
     v_out = np.array(v_cache, copy=True, order="C")
     k_new = np.ascontiguousarray(k_new)
     v_new = np.ascontiguousarray(v_new)
+    fp8 = _fp8_scales(k_scale, v_scale)
+    if fp8 is not None:
+        keep = []
+        dummy_q = np.zeros(batch.total_new_tokens * num_heads_kv * head_dim, dtype=k_new.dtype)
+        P = _problem(batch, dummy_q, k_new, v_new, k_out, v_out, num_heads_q=num_heads_kv,
+                     num_heads_kv=num_heads_kv, head_dim=head_dim, block_size=block_size, scale=1.0,
+                     mutation=mutation, keep=keep, kv_scales=fp8)
+        rc = lib.cpa_oracle_kv_write_fp8(ctypes.byref(P), k_out.ctypes.data, v_out.ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle kv_write (FP8) failed with status {rc}")
+        return k_out, v_out
     if k_new.dtype != k_out.dtype or v_new.dtype != v_out.dtype:
         raise TypeError("new rows and pools must share one element type")
     keep = []
@@ -249,3 +306,22 @@ def rope(batch: Batch, q, k_new, *, num_heads_q, num_heads_kv, head_dim, theta, 
     if rc != 0:
         raise RuntimeError(f"oracle rope failed with status {rc}")
     return q_out, k_out
+
+
+def e4m3_encode(y, mutation=MUT_NONE) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of float32 values: nearest, ties to an even
+    mantissa, |y| >= 448 saturated to +-448, NaN to the NaN code 0x7F."""
+    lib = _load()
+    y = np.ascontiguousarray(np.asarray(y, dtype=np.float32))
+    out = np.zeros(y.shape, dtype=np.uint8)
+    lib.cpa_oracle_e4m3_encode(y.ctypes.data, out.ctypes.data, ctypes.c_long(y.size), int(mutation))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of FP8 E4M3 codes."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    lib.cpa_oracle_e4m3_decode(c.ctypes.data, out.ctypes.data, ctypes.c_long(c.size))
+    return out

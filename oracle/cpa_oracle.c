@@ -43,6 +43,21 @@
  * dimension d at position p, each pair (x_c, x_{c+d/2}), c < d/2, turns by
  * the angle p * theta^(-2c/d).
  *
+ * FP8 key/value cache (optional, kv_fp8 = 1): "Prefill Processing" names a
+ * KV cache data representation (FP8 E4M3) with quantization scales as part
+ * of what makes cached KV reusable, and says nothing more.  The reading
+ * taken: the pools hold E4M3 codes (the OCP FP8 E4M3 format: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes the
+ * subnormals m * 2^-9; S.1111.111 is NaN; no infinities; largest finite
+ * value 448) with one fp32 scale per kv head for keys and one for values.
+ * An element x is stored as the code nearest to y = fl32(x / scale) (the
+ * quotient rounded to fp32, then rounded to nearest, ties to an even
+ * mantissa), saturated to +-448 when |y| >= 448; a NaN becomes the NaN
+ * code.  A code c stands for value(c) * scale.  Attention sees every key and
+ * value through this representation, the active tokens' own new rows
+ * included, so chunked prefill over the FP8 cache still equals one-shot
+ * attention over the quantized prompt.
+ *
  * Parity pins (see tests/test_oracle.py): closed forms (first token of a
  * fresh prompt returns v_0; zero queries give the mean of visible values;
  * constant values; one-hot scores), a pure-Python fsum brute force over the
@@ -77,6 +92,9 @@ typedef struct {
     const void *v_new;              /* [T, H_kv, d] */
     const void *k_cache;            /* [num_blocks, block_size, H_kv, d] */
     const void *v_cache;
+    int32_t kv_fp8;                 /* 1: pools hold FP8 E4M3 codes (uint8), see the header */
+    const float *k_scale;           /* [H_kv] key scales (kv_fp8 only) */
+    const float *v_scale;           /* [H_kv] value scales (kv_fp8 only) */
 } orc_problem;
 
 /* Planted mistakes, used only by the tests that prove the pins can fail. */
@@ -92,7 +110,52 @@ enum {
     MUT_WRITE_OFF_BY_ONE = 8,  /* KV write one slot too far */
     MUT_ROPE_INTERLEAVED = 9,  /* rotary pairs (2c, 2c+1) instead of (c, c + d/2) */
     MUT_ROPE_NO_OFFSET = 10,   /* rotary angle from i instead of cached_seq_len + i */
+    MUT_FP8_NEW_UNQUANTIZED = 11, /* FP8 cache: the active tokens' own keys/values skip the cache format */
+    MUT_FP8_HEAD0_SCALE = 12,  /* FP8 cache: every kv head uses head 0's scales */
+    MUT_FP8_TRUNCATE = 13,     /* FP8 encoder truncates instead of rounding to nearest */
 };
+
+/* Value of an FP8 E4M3 code (NaN for S.1111.111). */
+static double e4m3_value(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                /* subnormal: m * 2^-9 */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);         /* normal: 1.mmm * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+/* Code of an fp32 value: nearest representable value, ties to an even
+ * mantissa; |y| >= 448 saturates to +-448 (every value in [448, 464] rounds
+ * to 448, and larger ones clamp there); NaN gives the NaN code 0x7F. */
+static uint8_t e4m3_encode(float y, int mutation) {
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0;
+    const double a = fabs((double)y);
+    if (a >= 448.0) return sign | 0x7E;
+    int ex;
+    frexp(a, &ex);           /* a = f * 2^ex, f in [0.5, 1) */
+    int E = ex - 1;          /* a in [2^E, 2^(E+1)) */
+    if (E < -6) E = -6;      /* below the normal range the spacing stays 2^-9 */
+    const double quantum = ldexp(1.0, E - 3);            /* 3 mantissa bits */
+    const double n = (mutation == MUT_FP8_TRUNCATE) ? floor(a / quantum)
+                                                    : nearbyint(a / quantum); /* exact quotient; RNE */
+    const double v = n * quantum;                       /* may round up to 2^(E+1) */
+    if (v == 0.0) return sign;
+    frexp(v, &ex);
+    E = ex - 1;
+    if (E < -6) return sign | (uint8_t)(v / ldexp(1.0, -9));   /* subnormal code = m */
+    const int m = (int)(v / ldexp(1.0, E) * 8.0) - 8;
+    return sign | (uint8_t)((E + 7) << 3) | (uint8_t)m;
+}
+
+static float kv_scale(const orc_problem *P, int is_v, int g) {
+    const float *sc = is_v ? P->v_scale : P->k_scale;
+    return sc[P->mutation == MUT_FP8_HEAD0_SCALE ? 0 : g];
+}
 
 static double load_elem(const void *base, int dtype, size_t idx) {
     if (dtype == 0) return (double)((const float *)base)[idx];
@@ -124,11 +187,19 @@ static double kv_elem(const orc_problem *P, int is_v, int r, int j, int g, int c
             slot = (long)blk * bs + j % bs;
         }
         size_t idx = ((size_t)slot * hkv + g) * d + c;
+        if (P->kv_fp8)
+            return e4m3_value(((const uint8_t *)(is_v ? P->v_cache : P->k_cache))[idx]) * kv_scale(P, is_v, g);
         return load_elem(is_v ? P->v_cache : P->k_cache, P->dtype, idx);
     }
     int t = P->cu_new_tokens[r] + (j - C);
     size_t idx = ((size_t)t * hkv + g) * d + c;
-    return load_elem(is_v ? P->v_new : P->k_new, P->dtype, idx);
+    double x = load_elem(is_v ? P->v_new : P->k_new, P->dtype, idx);
+    if (P->kv_fp8 && P->mutation != MUT_FP8_NEW_UNQUANTIZED) {
+        /* the active token's own row, as the cache holds it */
+        const float sc = kv_scale(P, is_v, g);
+        x = e4m3_value(e4m3_encode((float)x / sc, P->mutation)) * sc;
+    }
+    return x;
 }
 
 typedef struct {
@@ -367,6 +438,45 @@ int cpa_oracle_kv_write(const orc_problem *P, int elem_bytes, void *k_cache, voi
         }
     }
     return 0;
+}
+
+/* The write into FP8 pools: every element of the active tokens' K/V rows is
+ * encoded with its kv head's scale (see the header) and stored as one byte
+ * in the slot row.  k_cache/v_cache are the oracle's own uint8 copies.
+ * Returns 0 or -3. */
+int cpa_oracle_kv_write_fp8(const orc_problem *P, uint8_t *k_cache, uint8_t *v_cache) {
+    if (!P || !k_cache || !v_cache || !P->k_scale || !P->v_scale) return -3;
+    const int hkv = P->num_heads_kv, d = P->head_dim;
+    for (int r = 0; r < P->num_reqs; ++r) {
+        int C = P->cached_seq_len[r];
+        for (int i = 0; i < P->num_new_tokens[r]; ++i) {
+            int pos = C + i;
+            if (P->mutation == MUT_WRITE_OFF_BY_ONE) pos += 1;
+            if (pos / P->block_size >= P->max_blocks_per_seq) return -3;
+            int blk = P->block_table[(size_t)r * P->max_blocks_per_seq + pos / P->block_size];
+            if (blk < 0 || blk >= P->num_blocks) return -3;
+            size_t slot = (size_t)blk * P->block_size + pos % P->block_size;
+            int t = P->cu_new_tokens[r] + i;
+            for (int g = 0; g < hkv; ++g)
+                for (int c = 0; c < d; ++c) {
+                    size_t src = ((size_t)t * hkv + g) * d + c, dst = (slot * hkv + g) * d + c;
+                    k_cache[dst] = e4m3_encode((float)load_elem(P->k_new, P->dtype, src) / kv_scale(P, 0, g),
+                                               P->mutation);
+                    v_cache[dst] = e4m3_encode((float)load_elem(P->v_new, P->dtype, src) / kv_scale(P, 1, g),
+                                               P->mutation);
+                }
+        }
+    }
+    return 0;
+}
+
+/* Element-wise E4M3 encode of fp32 values and decode of codes (for the
+ * tests of the format itself). */
+void cpa_oracle_e4m3_encode(const float *y, uint8_t *codes, long n, int mutation) {
+    for (long i = 0; i < n; ++i) codes[i] = e4m3_encode(y[i], mutation);
+}
+void cpa_oracle_e4m3_decode(const uint8_t *codes, double *out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
 }
 
 /* Rotary position embedding of the active tokens' queries and new keys
