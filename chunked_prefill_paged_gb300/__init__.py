@@ -20,6 +20,8 @@ from .binding import (  # noqa: F401
     FLAG_FUSE_KV_WRITE,
     FLAG_NO_SPLIT,
     FLAG_TEST_STALL,
+    KV_FP8_E4M3,
+    KV_SAME,
     LIB_PATH,
     SUCCESS,
     Batch,

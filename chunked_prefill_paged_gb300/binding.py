@@ -29,6 +29,9 @@ ERR_WORKSPACE = 6
 DTYPE_FP32 = 0
 DTYPE_BF16 = 1
 
+KV_SAME = 0
+KV_FP8_E4M3 = 1
+
 FLAG_FUSE_KV_WRITE = 0x1
 FLAG_FORCE_SIMT = 0x2
 FLAG_NO_SPLIT = 0x4
@@ -68,6 +71,9 @@ class _Params(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("timeout_cycles", ctypes.c_int64),
         ("rope_theta", ctypes.c_float),
+        ("kv_format", ctypes.c_int32),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -131,12 +137,20 @@ class Params:
     flags: int = FLAG_FUSE_KV_WRITE
     timeout_cycles: int = 0
     rope_theta: float = 0.0
+    # FP8 cache: kv_format KV_FP8_E4M3, uint8 pools, and float32 device
+    # tensors of H_kv scales for keys and for values
+    kv_format: int = KV_SAME
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
 
     def c(self) -> _Params:
         scale = self.scale if self.scale is not None else 1.0 / float(np.sqrt(self.head_dim))
+        for t in (self.k_scale, self.v_scale):
+            if t is not None and t.dtype != torch.float32:
+                raise TypeError("k_scale / v_scale must be float32 tensors")
         return _Params(self.num_heads_q, self.num_heads_kv, self.head_dim, self.block_size, self.num_blocks,
                        self.kv_segment_size, scale, self.dtype, self.flags, self.timeout_cycles,
-                       self.rope_theta)
+                       self.rope_theta, self.kv_format, _ptr(self.k_scale), _ptr(self.v_scale))
 
 
 class Batch:

@@ -60,7 +60,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;      // Q and K copies
 constexpr int kMmaWarp = 9;
@@ -71,17 +70,32 @@ constexpr int kSBuf = 3;              // score buffers in TMEM
 constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kUnitRing = 4;                // unit indices passed ahead to the other roles
-constexpr int kUnitReaders = 11;            // warps 0-7, 9, 10, 11 each read every index
+constexpr int kKConvWarp = 12;              // FP8 cache: warps 12-13 expand K tiles, 14-15 V tiles
 
-template <int D>
+// Threads and unit-ring readers of the two kernel flavours: BF16 pools (12
+// warps) and FP8 pools (16 warps: four more expand the codes).
+template <bool F8>
+struct TcRoles {
+    static constexpr int kThreads = F8 ? 512 : 384;
+    static constexpr int kUnitReaders = F8 ? 15 : 11;  // every warp but 8 reads every index
+};
+
+template <int D, bool F8>
 struct TcCfg {
     static constexpr int kHalves = D / 64;           // 64-element (128 B) column chunks
     static constexpr int kTileBytes = 128 * D * 2;   // 128 rows of D bf16 (Q, K or V tile)
     static constexpr int kHalfBytes = kTileBytes / kHalves;
     static constexpr int kQStages = 2;  // the next unit's Q loads while this one runs
-    static constexpr int kKStages = (D == 128) ? 3 : 6;
-    static constexpr int kVStages = (D == 128) ? 2 : 5;
-    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages);
+    // bf16 K / V rings the MMAs read.  With FP8 pools the copies land in
+    // separate rings of code tiles (128 rows x D bytes) that the expansion
+    // warps turn into these.
+    static constexpr int kKStages = F8 ? 2 : (D == 128) ? 3 : 6;
+    static constexpr int kVStages = F8 ? 1 : (D == 128) ? 2 : 5;
+    static constexpr int kCodeTileBytes = 128 * D;
+    static constexpr int kK8Stages = F8 ? 2 : 0;
+    static constexpr int kV8Stages = F8 ? 2 : 0;
+    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages) +
+                                      kCodeTileBytes * (kK8Stages + kV8Stages);
 };
 
 struct __align__(8) TcShared {
@@ -93,6 +107,8 @@ struct __align__(8) TcShared {
     uint64_t pv_done[kSBuf];  // per score buffer: the PV that read its P has completed
     uint64_t o_full, o_empty;
     uint64_t mma_done;
+    uint64_t k8_full[2], k8_empty[2];  // FP8 pools: code-tile rings
+    uint64_t v8_full[2], v8_empty[2];
     // unit scheduler: warp 8 takes unit indices from the launch's work
     // counter and passes them to the other roles through this ring
     uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
@@ -179,6 +195,65 @@ struct TileList {
     }
 };
 
+// Four E4M3 codes (bytes of w, lowest address first) as bf16: element pairs
+// (0, 1) in the first word, (2, 3) in the second, lower column in the low half.
+// From the two formats' layouts: a code s.eeee.mmm placed with its low seven
+// bits at bf16 bits 10..4 and its sign at bit 15 reads as the bf16 number
+// 2^-120 * value (the bf16 exponent bias is 127, the E4M3 one 7, and a code
+// with exponent field 0 lands on a bf16 subnormal with the same m * 2^-9
+// scaled by 2^-120); one exact bf16 multiply by 2^120 restores the value.
+// PRMT builds each 16-bit half as [sign byte | code] (selector nibbles with
+// bit 3 replicate a byte's sign), a shift by 4 moves the code to bits 11..4
+// and the mask keeps the sign and bits 10..4.
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));  // [S(b1) b1 S(b0) b0]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));  // [S(b3) b3 S(b2) b2]
+    a = (a << 4) & 0x87F087F0u;
+    b = (b << 4) & 0x87F087F0u;
+    constexpr uint32_t k2p120 = 0x7B807B80u;  // bf16 2^120 in both halves
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(k2p120));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(k2p120));
+}
+
+// Rows [r0, r0 + 64) of one 128 x 128 code tile (rows of 128 bytes) into the
+// bf16 tile the MMAs read: two 64-column halves of 128 rows x 128 B, 16-byte
+// chunk c of row r at chunk position c ^ (r % 8) (the 128-byte swizzle).
+// Rows at or past `valid` are written as zeros when zero_tail is set, else
+// left as they are.  Eight lanes share a row: lane piece p (16 codes, columns
+// 16p .. 16p + 15) fills chunks 2(p % 4) and 2(p % 4) + 1 of half p / 4.
+// Which of its two chunks a lane handles first alternates with the half and
+// with the row's parity: then every store instruction covers all eight chunk
+// positions of each row, and every 8-byte load instruction reads row pairs
+// whose byte ranges fall on complementary banks -- neither conflicts.
+__device__ __forceinline__ void expand_code_rows(const uint8_t *src, uint8_t *dst, int r0, int valid, bool zero_tail,
+                                                 int lane, int half_bytes) {
+    const int p = lane & 7;
+    const int h = p >> 2;
+    const int f = h ^ ((lane >> 3) & 1);  // r0 is even, so (lane >> 3) & 1 is the row's parity
+    const int c_first = 2 * (p & 3) + f, c_second = 2 * (p & 3) + 1 - f;
+#pragma unroll 4
+    for (int it = 0; it < 16; ++it) {
+        const int r = r0 + it * 4 + (lane >> 3);
+        uint8_t *row = dst + h * half_bytes + r * 128;
+        const int sw = r & 7;
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+        if (r < valid) {
+            const uint8_t *in = src + r * 128 + p * 16;
+            const uint2 w0 = *reinterpret_cast<const uint2 *>(in + 8 * f);        // codes of chunk c_first
+            const uint2 w1 = *reinterpret_cast<const uint2 *>(in + 8 * (1 - f));  // codes of chunk c_second
+            e4m3x4_to_bf16(w0.x, o0.x, o0.y);
+            e4m3x4_to_bf16(w0.y, o0.z, o0.w);
+            e4m3x4_to_bf16(w1.x, o1.x, o1.y);
+            e4m3x4_to_bf16(w1.y, o1.z, o1.w);
+        } else if (!zero_tail) {
+            continue;
+        }
+        *reinterpret_cast<uint4 *>(row + ((c_first ^ sw) << 4)) = o0;
+        *reinterpret_cast<uint4 *>(row + ((c_second ^ sw) << 4)) = o1;
+    }
+}
+
 // The i-th unit of this CTA, as published by the scheduling warp (every lane
 // of the calling warp takes part).  Returns a value >= the unit count when
 // the CTA is done, and -1 when the wait gave up (timeout or abort).
@@ -193,22 +268,26 @@ __device__ __forceinline__ int read_unit(TcShared &sh, int i, long long limit, c
     return unit;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k_new, const __grid_constant__ CUtensorMap tm_v_new,
                    const __grid_constant__ CUtensorMap tm_k_pool, const __grid_constant__ CUtensorMap tm_v_pool) {
-    using Cfg = TcCfg<D>;
+    using Cfg = TcCfg<D, F8>;
     constexpr int NSK = Cfg::kKStages;
     constexpr int NSV = Cfg::kVStages;
     constexpr int TB = Cfg::kTileBytes;
     constexpr int HB = Cfg::kHalfBytes;
+    constexpr int CB = Cfg::kCodeTileBytes;
+    static_assert(!F8 || D == 128, "FP8 pools: head_dim 128");
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcShared sh;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem;                // 2 stages
     uint8_t *sK = smem + Cfg::kQStages * TB;  // NSK stages
     uint8_t *sV = sK + NSK * TB;       // NSV stages
+    uint8_t *sK8 = sV + NSV * TB;      // FP8 pools: code tiles of K, then of V
+    uint8_t *sV8 = sK8 + Cfg::kK8Stages * CB;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -222,13 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.q_full[b], 1);
             mbar_init(&sh.q_empty[b], 1);
         }
+        // bf16 tiles: filled by one TMA arrival, or by the two expansion warps
         for (int s = 0; s < NSK; ++s) {
-            mbar_init(&sh.k_full[s], 1);
+            mbar_init(&sh.k_full[s], F8 ? 2 : 1);
             mbar_init(&sh.k_empty[s], 1);
         }
         for (int s = 0; s < NSV; ++s) {
-            mbar_init(&sh.v_full[s], 1);
+            mbar_init(&sh.v_full[s], F8 ? 2 : 1);
             mbar_init(&sh.v_empty[s], 1);
+        }
+        for (int s = 0; s < Cfg::kK8Stages; ++s) {
+            mbar_init(&sh.k8_full[s], 1);
+            mbar_init(&sh.k8_empty[s], 2);
+        }
+        for (int s = 0; s < Cfg::kV8Stages; ++s) {
+            mbar_init(&sh.v8_full[s], 1);
+            mbar_init(&sh.v8_empty[s], 2);
         }
         for (int b = 0; b < kSBuf; ++b) {
             mbar_init(&sh.s_full[b], 1);
@@ -240,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sh.mma_done, 2);  // one commit from each MMA warp
         for (int i = 0; i < kUnitRing; ++i) {
             mbar_init(&sh.unit_full[i], 1);
-            mbar_init(&sh.unit_empty[i], kUnitReaders);
+            mbar_init(&sh.unit_empty[i], TcRoles<F8>::kUnitReaders);
         }
         sh.abort_flag = 0;
         fence_mbar_init();
@@ -266,7 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ TMA
         const int kv_role = (warp == kVProducerWarp) ? 1 : 0;  // copies K (0) or V (1)
         bool ok = true;
-        const int ns = kv_role ? NSV : NSK;
+        // ring the copies go to: the bf16 tiles, or with FP8 pools the code tiles
+        const int ns = F8 ? (kv_role ? Cfg::kV8Stages : Cfg::kK8Stages) : (kv_role ? NSV : NSK);
+        uint64_t *const ring_full = F8 ? (kv_role ? sh.v8_full : sh.k8_full) : (kv_role ? sh.v_full : sh.k_full);
+        uint64_t *const ring_empty = F8 ? (kv_role ? sh.v8_empty : sh.k8_empty) : (kv_role ? sh.v_empty : sh.k_empty);
+        uint8_t *const ring = F8 ? (kv_role ? sV8 : sK8) : (kv_role ? sV : sK);
+        constexpr int slot_bytes = F8 ? CB : TB;
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
         int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
@@ -314,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *bt_row = a.bt + (long long)u.r * a.max_blocks;
             // copies of key tile j (K when kv = 0, V when kv = 1) into their ring slot
             auto load_kv = [&](int j, int kv) -> bool {
-                uint64_t *empty = kv ? &sh.v_empty[slot] : &sh.k_empty[slot];
-                uint64_t *full = kv ? &sh.v_full[slot] : &sh.k_full[slot];
-                uint8_t *dst = (kv ? sV : sK) + slot * TB;
+                uint64_t *empty = &ring_empty[slot];
+                uint64_t *full = &ring_full[slot];
+                uint8_t *dst = ring + slot * slot_bytes;
                 if (!__all_sync(0xffffffffu, mbar_wait_or_abort(empty, ph ^ 1u, LIM, abort_flag))) return false;
                 int key0, valid;
                 bool pooled;
@@ -324,7 +417,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (a.test_stall && it == 0 && j == 0 && kv == 0) {
                     // testing only: arm the barrier but never copy, so the
                     // MMA warp's bounded wait on this tile expires
-                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)TB);
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)slot_bytes);
+                } else if (F8 && pooled) {
+                    // code tile: one box of bs rows x D bytes per cache block
+                    const int nblk = cdiv(valid, a.bs);
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * a.bs * D));
+                    __syncwarp();
+                    const int col0 = key0 / a.bs;
+                    for (int b = lane; b < nblk; b += 32) {
+                        int blk = __ldg(bt_row + col0 + b);
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            record_error(a.err, kErrBadBlock);
+                            blk = 0;  // keep the byte count; this unit's output is void
+                        }
+                        tma_load_4d(dst + b * a.bs * D, kv ? &tm_v_pool : &tm_k_pool, full, 0, u.g, 0, blk);
+                    }
+                } else if (F8) {
+                    // the new rows' codes: one 128-row box of the workspace copy
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)CB);
+                    __syncwarp();
+                    if (lane == 0)
+                        tma_load_3d(dst, kv ? &tm_v_new : &tm_k_new, full, 0, u.g, u.cu0 + (key0 - u.C));
                 } else if (pooled) {
                     const int nblk = cdiv(valid, a.bs);
                     if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * a.bs * D * 2));
@@ -391,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st += ns;
                 p ^= 1u;
             }
-            mbar_wait(kv_role ? &sh.v_full[st] : &sh.k_full[st], p, LIM);
+            mbar_wait(&ring_full[st], p, LIM);
         }
         __syncwarp();
     } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -495,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int key0, valid;
                     bool pooled;
                     tl.tile(j, key0, valid, pooled);
-                    if (valid < kKT) {
+                    if (!F8 && valid < kKT) {
                         // keys past the tile's valid range: zero their V rows so
                         // that P = 0 never meets a NaN or Inf left in the pool or
                         // in this ring slot (16 bytes per lane; then a proxy fence,
@@ -539,13 +652,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_warp(&sh.mma_done);
         mbar_wait(&sh.mma_done, 0, LIM);
         __syncwarp();
+    } else if (F8 && warp >= kKConvWarp) {
+        // ==================================== FP8 expansion (warps 12-15)
+        // Warps 12-13 turn K code tiles into bf16 K tiles, 14-15 V tiles; each
+        // warp takes 64 rows.  V rows past a tile's valid keys become zeros
+        // (P = 0 must not meet a NaN code left in the pool or the ring); K
+        // rows there are left as they are, the softmax masks their scores.
+        const int kv = (warp - kKConvWarp) >> 1;
+        const int r0 = ((warp - kKConvWarp) & 1) * 64;
+        const int ns8 = kv ? Cfg::kV8Stages : Cfg::kK8Stages;
+        const int nsb = kv ? NSV : NSK;
+        int s8 = 0, sb = 0;
+        uint32_t ph8 = 0, phb = 0;
+        bool ok = true;
+        for (int cc = 0;; ++cc) {
+            const int unit = read_unit(sh, cc, LIM, abort_flag);
+            if (unit < 0) {
+                ok = false;
+                break;
+            }
+            if (unit >= end_index) break;
+            if (unit >= total_units) continue;
+            if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
+            Unit u;
+            decode_unit(a, unit, u);
+            TileList tl;
+            tl.init(u);
+            for (int j = 0; j < tl.n_total; ++j) {
+                uint64_t *code_full = kv ? &sh.v8_full[s8] : &sh.k8_full[s8];
+                uint64_t *code_empty = kv ? &sh.v8_empty[s8] : &sh.k8_empty[s8];
+                uint64_t *bf_full = kv ? &sh.v_full[sb] : &sh.k_full[sb];
+                uint64_t *bf_empty = kv ? &sh.v_empty[sb] : &sh.k_empty[sb];
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bf_empty, phb ^ 1u, LIM, abort_flag)) ||
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(code_full, ph8, LIM, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                int key0, valid;
+                bool pooled;
+                tl.tile(j, key0, valid, pooled);
+                expand_code_rows((kv ? sV8 : sK8) + s8 * CB, (kv ? sV : sK) + sb * TB, r0, valid, kv == 1, lane, HB);
+                fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bf_full);
+                    mbar_arrive(code_empty);
+                }
+                if (++s8 == ns8) {
+                    s8 = 0;
+                    ph8 ^= 1u;
+                }
+                if (++sb == nsb) {
+                    sb = 0;
+                    phb ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        if (!ok) {
+            if (lane == 0) record_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
+        __syncwarp();
     } else if (warp < 8) {
         // ============================================== softmax (warps 0-7)
         const int half = lane >> 4;                                // 0: keys 0-63, 1: keys 64-127
         const int lr = 32 * (warp & 3) + 16 * (warp >> 2) + (lane & 15);  // row of the tile == TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3) + 16 * (warp >> 2)) << 16);
         const uint32_t tO = lane_base + kTmemO;
-        const float sl = a.scale_log2;
+        float sl = a.scale_log2;  // with FP8 pools times the unit's key scale
         int cb = 0;          // score buffer of the next tile
         uint32_t cph = 0;    // and its use parity
         int prev_b = 0;      // buffer and use parity of the previous tile (for the PV(j-1) wait)
@@ -577,6 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = tl.n_total;
             const bool row_valid = lr < u.rows;
             const int pos = row_valid ? u.C + (u.row0 + lr) / a.G : -1;
+            // FP8 pools: the tiles hold code values; a key's scale multiplies
+            // every score of the unit (one kv head), a value's scale the output
+            float v_mul = 1.f;
+            if (F8) {
+                sl = a.scale_log2 * __ldg(a.k_scale + u.g);
+                v_mul = __ldg(a.v_scale + u.g);
+            }
             float m_ref = -INFINITY, l = 0.f;
             // a warp whose 16 rows are all padding (a decode has G rows of
             // 128) skips the math; each O row depends on its own P row only,
@@ -698,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l += __shfl_xor_sync(0xffffffffu, l, 16);  // whole row
             // epilogue: this thread's half of the O row, then release O
             const int pr = u.row0 + lr;  // packed row of the request
-            const float inv = 1.f / l;
+            const float inv = v_mul / l;
             const int t = u.cu0 + pr / a.G, h = u.g * a.G + pr % a.G;
 #pragma unroll
             for (int c = 0; c < D / 64 && warp_rows; ++c) {
@@ -711,8 +893,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float4 *dst = reinterpret_cast<float4 *>(a.ws + u.ws_off + (long long)pr * D + col0);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]) * v_mul, __uint_as_float(r[4 * i + 1]) * v_mul,
+                                                 __uint_as_float(r[4 * i + 2]) * v_mul,
+                                                 __uint_as_float(r[4 * i + 3]) * v_mul);
                     } else {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
                                                                ((long long)t * a.hq + h) * D + col0);
@@ -754,24 +937,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int D, bool F8>
+cudaError_t launch_tc(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_t stream) {
+    constexpr int smem = TcCfg<D, F8>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<D, F8><<<grid, TcRoles<F8>::kThreads, smem, stream>>>(a, m.q, m.k_new, m.v_new, m.k_pool,
+                                                                          m.v_pool);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attn_tc(const AttnArgs &a, const TcMaps &m, cudaStream_t stream) {
-    const int grid = a.write_ctas;  // persistent: min(units, SMs)
+    const int grid = a.write_ctas;  // persistent: min(units + write pieces, SMs)
     if (grid <= 0 || a.num_direct_units + a.num_split_units == 0) return cudaSuccess;
-    cudaError_t e;
-    if (a.d == 128) {
-        constexpr int smem = TcCfg<128>::kSmemBytes;
-        e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<128><<<grid, kThreads, smem, stream>>>(a, m.q, m.k_new, m.v_new, m.k_pool, m.v_pool);
-    } else {
-        constexpr int smem = TcCfg<64>::kSmemBytes;
-        e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<64><<<grid, kThreads, smem, stream>>>(a, m.q, m.k_new, m.v_new, m.k_pool, m.v_pool);
-    }
-    return cudaGetLastError();
+    if (a.kv_fp8) return a.d == 128 ? launch_tc<128, true>(a, m, grid, stream) : cudaErrorInvalidValue;
+    return a.d == 128 ? launch_tc<128, false>(a, m, grid, stream) : launch_tc<64, false>(a, m, grid, stream);
 }
 
 }  // namespace cpa

@@ -84,6 +84,13 @@ cpa_status validate(const cpa_batch *b, const cpa_params *p) {
     if (!isfinite(p->scale) || !(p->scale > 0.f)) return CPA_ERR_INVALID_ARG;
     if (!isfinite(p->rope_theta) || p->rope_theta < 0.f) return CPA_ERR_INVALID_ARG;
     if (p->timeout_cycles < 0) return CPA_ERR_INVALID_ARG;
+    if (p->kv_format != CPA_KV_SAME && p->kv_format != CPA_KV_FP8_E4M3) return CPA_ERR_INVALID_ARG;
+    if (p->kv_format == CPA_KV_FP8_E4M3) {
+        if (!p->k_scale || !p->v_scale || (reinterpret_cast<uintptr_t>(p->k_scale) & 3u) ||
+            (reinterpret_cast<uintptr_t>(p->v_scale) & 3u))
+            return CPA_ERR_INVALID_ARG;
+        if (p->dtype != CPA_DTYPE_BF16) return CPA_ERR_UNSUPPORTED;  // FP8 codes of BF16 rows only
+    }
     if (b->num_reqs < 0 || b->total_new_tokens < 0) return CPA_ERR_INVALID_ARG;
     if (b->num_reqs == 0) return b->total_new_tokens == 0 ? CPA_SUCCESS : CPA_ERR_INVALID_ARG;
     if (b->max_blocks_per_seq <= 0) return CPA_ERR_INVALID_ARG;
@@ -101,6 +108,8 @@ cpa_status validate(const cpa_batch *b, const cpa_params *p) {
     return CPA_SUCCESS;
 }
 
+bool kv_fp8(const cpa_params *p) { return p->kv_format == CPA_KV_FP8_E4M3; }
+
 bool use_tensor_cores(const cpa_params *p) {
     if (p->dtype != CPA_DTYPE_BF16) return false;
     if (p->flags & CPA_FLAG_FORCE_SIMT) return false;
@@ -115,6 +124,7 @@ struct Plan {
     int head_major = 0;
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
     size_t rq_off = 0, rk_off = 0;  // rotated q / k_new copies (rope_theta > 0)
+    size_t kq_off = 0, vq_off = 0;  // FP8 cache: codes of k_new / v_new
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
     int direct_units = 0;
@@ -124,6 +134,13 @@ struct Plan {
 };
 
 int elem_bytes(const cpa_params *p) { return p->dtype == CPA_DTYPE_FP32 ? 4 : 2; }
+int pool_elem_bytes(const cpa_params *p) { return kv_fp8(p) ? 1 : elem_bytes(p); }
+
+// Attention over FP8 pools runs on the tensor-core kernel only (d = 128).
+cpa_status check_attention_support(const cpa_params *p) {
+    if (kv_fp8(p) && (p->head_dim != 128 || !use_tensor_cores(p))) return CPA_ERR_UNSUPPORTED;
+    return CPA_SUCCESS;
+}
 
 Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     Plan pl;
@@ -141,18 +158,27 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
         pl.split_reqs += w.split_units > 0 ? 1 : 0;
         pl.ws_floats += w.ws_floats;
         kv_bytes += (double)(b->h_cached_seq_len[r] + b->h_num_new_tokens[r]) * p->num_heads_kv * p->head_dim * 2.0 *
-                    elem_bytes(p);
+                    pool_elem_bytes(p);
     }
     // K/V of the batch larger than about half of L2: walk the direct units
     // head by head so that concurrent CTAs share K/V tiles in L2
     pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
     pl.ws_bytes = (size_t)pl.ws_floats * sizeof(float);
+    const size_t T = (size_t)b->total_new_tokens, es = (size_t)elem_bytes(p), d = (size_t)p->head_dim;
+    auto take = [&](size_t bytes) {  // next 256-byte aligned part of the workspace
+        const size_t off = (pl.ws_bytes + 255) & ~(size_t)255;
+        pl.ws_bytes = off + bytes;
+        return off;
+    };
     if (p->rope_theta > 0.f) {
-        // rotated copies of q and k_new, which the attention then reads
-        const size_t T = (size_t)b->total_new_tokens, es = (size_t)elem_bytes(p), d = (size_t)p->head_dim;
-        pl.rq_off = (pl.ws_bytes + 255) & ~(size_t)255;
-        pl.rk_off = (pl.rq_off + T * p->num_heads_q * d * es + 255) & ~(size_t)255;
-        pl.ws_bytes = pl.rk_off + T * p->num_heads_kv * d * es;
+        // rotated copies of q and (plain pools) k_new, which the attention then reads
+        pl.rq_off = take(T * p->num_heads_q * d * es);
+        if (!kv_fp8(p)) pl.rk_off = take(T * p->num_heads_kv * d * es);
+    }
+    if (kv_fp8(p)) {
+        // the new rows as the FP8 cache holds them, read by the attention
+        pl.kq_off = take(T * p->num_heads_kv * d);
+        pl.vq_off = take(T * p->num_heads_kv * d);
     }
     if (tc) {
         // the persistent kernel's work counter, after the partials
@@ -163,14 +189,17 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
 }
 
 
+// bf16 tiles land 128-byte swizzled (the MMA operand layout); FP8 code tiles
+// land as plain rows for the expansion warps
 cpa_status encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                  const cuuint32_t *box) {
+                  const cuuint32_t *box, bool codes = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return CPA_ERR_CUDA;
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                     const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? CPA_SUCCESS : CPA_ERR_CUDA;
 }
 
@@ -185,6 +214,20 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
         const cuuint32_t box[3] = {64, G, (cuuint32_t)kTcTileM / G};
         if (cpa_status s = encode(&m.q, q, 3, dims, strides, box)) return s;
     }
+    const cuuint32_t box_rows = (cuuint32_t)(bs < (cuuint64_t)kTcTileN ? bs : (cuuint64_t)kTcTileN);
+    if (kv_fp8(p)) {
+        // codes: one byte per element, a box spans the whole d-byte head row
+        const cuuint64_t dims3[3] = {D, Hkv, T};
+        const cuuint64_t strides3[2] = {D, Hkv * D};
+        const cuuint32_t box3[3] = {(cuuint32_t)D, 1, (cuuint32_t)kTcTileN};
+        if (cpa_status s = encode(&m.k_new, k_new, 3, dims3, strides3, box3, true)) return s;
+        if (cpa_status s = encode(&m.v_new, v_new, 3, dims3, strides3, box3, true)) return s;
+        const cuuint64_t dims4[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
+        const cuuint64_t strides4[3] = {D, Hkv * D, bs * Hkv * D};
+        const cuuint32_t box4[4] = {(cuuint32_t)D, 1, box_rows, 1};
+        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims4, strides4, box4, true)) return s;
+        return encode(&m.v_pool, v_cache, 4, dims4, strides4, box4, true);
+    }
     {
         const cuuint64_t dims[3] = {D, Hkv, T};
         const cuuint64_t strides[2] = {D * 2, Hkv * D * 2};
@@ -195,8 +238,7 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
     {
         const cuuint64_t dims[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
         const cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
-        // one box is one block, or the half of a 128-token block that one key tile covers
-        const cuuint32_t box_rows = (cuuint32_t)(bs < (cuuint64_t)kTcTileN ? bs : (cuuint64_t)kTcTileN);
+        // one box is one block (or the 128 rows of a block one key tile covers)
         const cuuint32_t box[4] = {64, 1, box_rows, 1};
         if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims, strides, box)) return s;
         if (cpa_status s = encode(&m.v_pool, v_cache, 4, dims, strides, box)) return s;
@@ -218,7 +260,11 @@ RopeArgs rope_args(const cpa_batch *batch, const cpa_params *params, int *err) {
     r.bs = params->block_size;
     r.num_blocks = params->num_blocks;
     r.elem_bytes = elem_bytes(params);
-    for (int c = 0; c < params->head_dim / 2; ++c) {
+    r.rotate = params->rope_theta > 0.f ? 1 : 0;
+    r.kv_fp8 = kv_fp8(params) ? 1 : 0;
+    r.k_scale = params->k_scale;
+    r.v_scale = params->v_scale;
+    for (int c = 0; c < params->head_dim / 2 && r.rotate; ++c) {
         const double turns = pow((double)params->rope_theta, -2.0 * c / params->head_dim) / 6.283185307179586477;
         r.turn_frac[c] = (unsigned long long)ldexp(turns, 64);  // turns < 1 / (2 pi): fits
     }
@@ -250,6 +296,7 @@ const char *cpa_status_string(cpa_status s) {
 
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params) {
     if (validate(batch, params) != CPA_SUCCESS || batch->num_reqs == 0) return 0;
+    if (check_attention_support(params) != CPA_SUCCESS) return 0;
     const Plan pl = make_plan(batch, params);
     return pl.ws_bytes;
 }
@@ -263,8 +310,9 @@ cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, cons
         return CPA_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (cpa_status s = device_info(dev)) return s;
-    if (params->rope_theta > 0.f) {
-        // rotated keys and the values go to the pool; no rotated copies are kept
+    if (params->rope_theta > 0.f || kv_fp8(params)) {
+        // rotated keys (and the values) go to the pool, as E4M3 codes with the
+        // FP8 cache; no copies are kept
         RopeArgs r = rope_args(batch, params, dev.err);
         r.k_new = k_new;
         r.v_new = v_new;
@@ -301,6 +349,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
         !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return CPA_ERR_INVALID_ARG;
+    if (cpa_status s = check_attention_support(params)) return s;
     const Plan pl = make_plan(batch, params);
     const size_t need = pl.ws_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CPA_ERR_WORKSPACE;
@@ -308,21 +357,30 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     if (cpa_status s = device_info(dev)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
-    if (params->rope_theta > 0.f) {
-        // rotate q and k_new into the workspace (and, for a fused write, put the
-        // rotated keys and the values into the pool); the attention reads the copies
+    if (params->rope_theta > 0.f || kv_fp8(params)) {
+        // pre-pass over the new rows: rotate q and k_new, encode the keys and
+        // values for the FP8 cache, into workspace copies that the attention
+        // then reads (and, for a fused write, put the rows as the pool holds
+        // them into their slots)
+        char *ws = static_cast<char *>(workspace);
         RopeArgs r = rope_args(batch, params, dev.err);
         r.q = q;
         r.k_new = k_new;
         r.v_new = v_new;
-        r.q_rot = static_cast<char *>(workspace) + pl.rq_off;
-        r.k_rot = static_cast<char *>(workspace) + pl.rk_off;
+        r.q_rot = r.rotate ? ws + pl.rq_off : nullptr;
+        r.k_rot = (r.rotate && !r.kv_fp8) ? ws + pl.rk_off : nullptr;
+        r.k_q8 = r.kv_fp8 ? ws + pl.kq_off : nullptr;
+        r.v_q8 = r.kv_fp8 ? ws + pl.vq_off : nullptr;
         r.write_pool = fuse_write ? 1 : 0;
         r.k_cache = k_cache;
         r.v_cache = v_cache;
         if (launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
-        q = r.q_rot;
-        k_new = r.k_rot;
+        if (r.q_rot) q = r.q_rot;
+        if (r.k_rot) k_new = r.k_rot;
+        if (r.kv_fp8) {
+            k_new = r.k_q8;
+            v_new = r.v_q8;
+        }
         fuse_write = false;
     }
 
@@ -369,6 +427,9 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.err = dev.err;
     a.timeout_cycles = params->timeout_cycles > 0 ? params->timeout_cycles : kDefaultTimeoutCycles;
     a.test_stall = (params->flags & CPA_FLAG_TEST_STALL) ? 1 : 0;
+    a.kv_fp8 = kv_fp8(params) ? 1 : 0;
+    a.k_scale = params->k_scale;
+    a.v_scale = params->v_scale;
 
     cudaError_t e;
     if (pl.tile_m == kTcTileM) {

@@ -115,12 +115,19 @@ struct AttnArgs {
     int *err;           // device error word (first error wins)
     long long timeout_cycles;
     int test_stall;     // testing only: withhold the first K tile's copies
+    // FP8 cache: pools and k_new / v_new (the workspace copies of the new rows'
+    // codes) hold E4M3 codes; a code of kv head g stands for value * scale[g]
+    int kv_fp8;
+    const float *k_scale;  // [hkv]
+    const float *v_scale;  // [hkv]
 };
 
-// Arguments of the rotary pre-pass: rotates the active tokens' queries and
-// new keys at absolute position cached[r] + i (pairs (c, c + d/2) turned by
-// p * theta^(-2c/d)) into q_rot / k_rot, and with write_pool also stores the
-// rotated keys and the values into their pool slots.
+// Arguments of the pre-pass over the active tokens' rows: with rotate, turns
+// queries and new keys at absolute position cached[r] + i (pairs (c, c + d/2)
+// by p * theta^(-2c/d)) into q_rot / k_rot; with kv_fp8, encodes the (rotated)
+// keys and the values as E4M3 codes into k_q8 / v_q8; with write_pool, stores
+// the keys and values (rotated, encoded as the pool holds them) into their
+// pool slots.
 struct RopeArgs {
     int num_reqs, max_blocks, total_tokens;
     const int32_t *cached;
@@ -140,6 +147,12 @@ struct RopeArgs {
     void *k_cache;
     void *v_cache;
     int *err;
+    int rotate;           // 0: keys pass unrotated (turn_frac unused)
+    int kv_fp8;           // pools hold E4M3 codes (element type bf16)
+    const float *k_scale; // [hkv]
+    const float *v_scale; // [hkv]
+    void *k_q8;           // [T, hkv, d] codes of the keys, or null
+    void *v_q8;           // [T, hkv, d] codes of the values, or null
 };
 
 // Arguments of the standalone KV write.

@@ -10,6 +10,7 @@
 // carried across key tiles (online softmax), in the log2 domain: scores are
 // multiplied by scale * log2(e) and exponentiated with exp2.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,23 +38,48 @@ cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stre
     return cudaGetLastError();
 }
 
-// ------------------------------------------------------------ rotary pre-pass
+// ------------------------------------------------ rotary / FP8 pre-pass
 // One warp per (active token, group of kHeadsPerWarp heads; query heads first,
-// then key heads).  The angle of pair c is reduced to one turn exactly in
-// integer arithmetic: turn_frac[c] holds theta^(-2c/d) / (2 pi) as a 64-bit
-// binary fraction, so pos * turn_frac[c] modulo 2^64 (a wrapping 64-bit
-// product) is the fraction of a turn; its top 24 bits give the angle in
-// [0, 2 pi), whose cosine and sine are taken in fp32.  The rotation runs in
-// fp32 and is rounded to the element type.  Lane l owns pairs c = 2l, 2l + 1
-// (d = 128) or c = l (d = 64), so the warp's accesses to each half row are
-// contiguous.
+// then key heads; query heads only when rotated queries are wanted).
+//
+// Rotation: the angle of pair c is reduced to one turn exactly in integer
+// arithmetic: turn_frac[c] holds theta^(-2c/d) / (2 pi) as a 64-bit binary
+// fraction, so pos * turn_frac[c] modulo 2^64 (a wrapping 64-bit product) is
+// the fraction of a turn; its top 24 bits give the angle in [0, 2 pi), whose
+// cosine and sine are taken in fp32.  The rotation runs in fp32 and is
+// rounded to the element type.
+//
+// FP8 cache: each key (after rotation, as the element type) and value
+// element x of kv head g becomes the E4M3 code of fl32(x / scale[g]) --
+// correctly rounded division, then the hardware conversion, round to
+// nearest even with saturation to +-448.
+//
+// Lane l owns pairs c = 2l, 2l + 1 (d = 128) or c = l (d = 64), so the warp's
+// accesses to each half row are contiguous.
 constexpr int kHeadsPerWarp = 8;
 
 // PPL consecutive elements of a lane moved as one access
 template <int BYTES> struct LaneVec;
+template <> struct LaneVec<1> { using type = unsigned char; };
 template <> struct LaneVec<2> { using type = unsigned short; };
 template <> struct LaneVec<4> { using type = unsigned int; };
 template <> struct LaneVec<8> { using type = uint2; };
+
+__device__ __forceinline__ uint8_t e4m3_code(float x, float scale) {
+    return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+}
+
+// the PPL codes of a lane's elements, packed as they lie in memory
+template <int PPL, typename T>
+__device__ __forceinline__ typename LaneVec<PPL>::type e4m3_lane(const T (&e)[PPL], float scale) {
+    union {
+        typename LaneVec<PPL>::type v;
+        uint8_t b[PPL];
+    } c;
+#pragma unroll
+    for (int i = 0; i < PPL; ++i) c.b[i] = e4m3_code(to_float(e[i]), scale);
+    return c.v;
+}
 
 template <int D, typename T>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
@@ -63,8 +89,9 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     for (int c = threadIdx.x; c < HALF; c += blockDim.x) frac_s[c] = a.turn_frac[c];
     __syncthreads();
     const int lane = threadIdx.x & 31;
+    const int head_lo = a.q_rot ? 0 : a.hq;  // without rotated queries only key heads
     const int heads = a.hq + a.hkv;
-    const int groups = (heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const int groups = (heads - head_lo + kHeadsPerWarp - 1) / kHeadsPerWarp;
     const long long wid = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
     if (wid >= (long long)a.total_tokens * groups) return;
     const int t = (int)(wid / groups), grp = (int)(wid % groups);
@@ -73,48 +100,81 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     float cs[PPL], sn[PPL];
 #pragma unroll
     for (int e = 0; e < PPL; ++e) {
-        const unsigned long long turn = (unsigned long long)pos * frac_s[lane * PPL + e];  // wraps: mod 1 turn
-        const float ang = (float)(turn >> 40) * (6.28318530717958648f / 16777216.0f);
-        sincosf(ang, &sn[e], &cs[e]);
+        cs[e] = 1.f;
+        sn[e] = 0.f;
+        if (a.rotate) {
+            const unsigned long long turn = (unsigned long long)pos * frac_s[lane * PPL + e];  // wraps: mod 1 turn
+            const float ang = (float)(turn >> 40) * (6.28318530717958648f / 16777216.0f);
+            sincosf(ang, &sn[e], &cs[e]);
+        }
     }
     long long slot = -1;
     if (a.write_pool) slot = slot_of(a.bt, a.max_blocks, a.bs, a.num_blocks, r, pos, a.err);
-    const int h_end = min(heads, (grp + 1) * kHeadsPerWarp);
-    for (int head = grp * kHeadsPerWarp; head < h_end; ++head) {
+    using V = typename LaneVec<PPL * (int)sizeof(T)>::type;
+    using C8 = typename LaneVec<PPL>::type;
+    union Lane {
+        V v;
+        T e[PPL];
+    };
+    const int h_begin = head_lo + grp * kHeadsPerWarp;
+    const int h_end = min(heads, h_begin + kHeadsPerWarp);
+    for (int head = h_begin; head < h_end; ++head) {
         const bool is_q = head < a.hq;
-        if (is_q && a.q_rot == nullptr) continue;
         const int hh = is_q ? head : head - a.hq;
         const long long row = ((long long)t * (is_q ? a.hq : a.hkv) + hh) * D;
-        using V = typename LaneVec<PPL * (int)sizeof(T)>::type;
         const T *src = static_cast<const T *>(is_q ? a.q : a.k_new) + row + lane * PPL;
-        union {
-            V v;
-            T e[PPL];
-        } xl, xh;
+        Lane xl, xh;
         xl.v = *reinterpret_cast<const V *>(src);
         xh.v = *reinterpret_cast<const V *>(src + HALF);
+        if (a.rotate) {
 #pragma unroll
-        for (int e = 0; e < PPL; ++e) {
-            const float x0 = to_float(xl.e[e]), x1 = to_float(xh.e[e]);
-            xl.e[e] = from_float<T>(x0 * cs[e] - x1 * sn[e]);
-            xh.e[e] = from_float<T>(x1 * cs[e] + x0 * sn[e]);
+            for (int e = 0; e < PPL; ++e) {
+                const float x0 = to_float(xl.e[e]), x1 = to_float(xh.e[e]);
+                xl.e[e] = from_float<T>(x0 * cs[e] - x1 * sn[e]);
+                xh.e[e] = from_float<T>(x1 * cs[e] + x0 * sn[e]);
+            }
         }
-        T *dst = nullptr;
-        if (is_q) dst = static_cast<T *>(a.q_rot) + row;
-        else if (a.k_rot) dst = static_cast<T *>(a.k_rot) + row;
-        T *kp = (!is_q && slot >= 0) ? static_cast<T *>(a.k_cache) + (slot * a.hkv + hh) * D : nullptr;
-        if (dst) {
+        if (is_q) {
+            T *dst = static_cast<T *>(a.q_rot) + row;
             *reinterpret_cast<V *>(dst + lane * PPL) = xl.v;
             *reinterpret_cast<V *>(dst + HALF + lane * PPL) = xh.v;
+            continue;
         }
-        if (kp) {
-            *reinterpret_cast<V *>(kp + lane * PPL) = xl.v;
-            *reinterpret_cast<V *>(kp + HALF + lane * PPL) = xh.v;
+        const long long prow = slot >= 0 ? (slot * a.hkv + hh) * D : -1;  // pool row of this head
+        if (!a.kv_fp8) {
+            if (a.k_rot) {
+                T *dst = static_cast<T *>(a.k_rot) + row;
+                *reinterpret_cast<V *>(dst + lane * PPL) = xl.v;
+                *reinterpret_cast<V *>(dst + HALF + lane * PPL) = xh.v;
+            }
+            if (prow >= 0) {
+                T *kp = static_cast<T *>(a.k_cache) + prow;
+                *reinterpret_cast<V *>(kp + lane * PPL) = xl.v;
+                *reinterpret_cast<V *>(kp + HALF + lane * PPL) = xh.v;
+                // the value row goes to the same slot unchanged, 16 bytes per lane
+                const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + row);
+                uint4 *vp = reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + prow);
+                for (int c = lane; c < D * (int)sizeof(T) / 16; c += 32) vp[c] = vs[c];
+            }
+            continue;
         }
-        if (kp) {  // the value row goes to the same slot unchanged, 16 bytes per lane
-            const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + row);
-            uint4 *vp = reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + (slot * a.hkv + hh) * D);
-            for (int c = lane; c < D * (int)sizeof(T) / 16; c += 32) vp[c] = vs[c];
+        // FP8 cache: codes of the key and of the value elements this lane owns
+        const float ks = __ldg(a.k_scale + hh), vsc = __ldg(a.v_scale + hh);
+        const C8 kl = e4m3_lane<PPL>(xl.e, ks), kh = e4m3_lane<PPL>(xh.e, ks);
+        Lane yl, yh;
+        const T *vsrc = static_cast<const T *>(a.v_new) + row + lane * PPL;
+        yl.v = *reinterpret_cast<const V *>(vsrc);
+        yh.v = *reinterpret_cast<const V *>(vsrc + HALF);
+        const C8 vl = e4m3_lane<PPL>(yl.e, vsc), vh = e4m3_lane<PPL>(yh.e, vsc);
+        uint8_t *dsts[4] = {a.k_q8 ? static_cast<uint8_t *>(a.k_q8) + row : nullptr,
+                            a.v_q8 ? static_cast<uint8_t *>(a.v_q8) + row : nullptr,
+                            prow >= 0 ? static_cast<uint8_t *>(a.k_cache) + prow : nullptr,
+                            prow >= 0 ? static_cast<uint8_t *>(a.v_cache) + prow : nullptr};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!dsts[i]) continue;
+            *reinterpret_cast<C8 *>(dsts[i] + lane * PPL) = (i & 1) ? vl : kl;
+            *reinterpret_cast<C8 *>(dsts[i] + HALF + lane * PPL) = (i & 1) ? vh : kh;
         }
     }
 }
@@ -123,7 +183,8 @@ cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (a.total_tokens == 0) return cudaSuccess;
     const int warps = 8;
-    const long long work = (long long)a.total_tokens * ((a.hq + a.hkv + kHeadsPerWarp - 1) / kHeadsPerWarp);
+    const int heads = a.q_rot ? a.hq + a.hkv : a.hkv;
+    const long long work = (long long)a.total_tokens * ((heads + kHeadsPerWarp - 1) / kHeadsPerWarp);
     const int blocks = (int)((work + warps - 1) / warps);
     if (a.elem_bytes == 2) {
         if (a.d == 128)

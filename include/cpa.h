@@ -26,8 +26,9 @@
  *     the absolute position offset of each chunk.
  *
  * Conventions shared by every entry point:
- *   - Element type: CPA_DTYPE_BF16 or CPA_DTYPE_FP32; q, k_new, v_new, the
- *     pools and out share it.
+ *   - Element type: CPA_DTYPE_BF16 or CPA_DTYPE_FP32; q, k_new, v_new and
+ *     out share it, and so do the pools unless kv_format selects the FP8
+ *     cache (below).
  *   - q     [T, H_q, d]   contiguous, rows packed by request (cu_new_tokens).
  *   - k_new [T, H_kv, d]  contiguous; v_new likewise.
  *   - out   [T, H_q, d]   contiguous.
@@ -39,6 +40,21 @@
  *       + p % block_size,
  *     and a slot is one row of the pool.
  *   - Query head h reads key/value head h / (H_q / H_kv).
+ *   - FP8 cache (kv_format = CPA_KV_FP8_E4M3): the pools hold one byte per
+ *     element, an FP8 E4M3 code (OCP format: sign, 4 exponent bits with bias
+ *     7, 3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9;
+ *     S.1111.111 is NaN; largest finite value 448), with one float scale per
+ *     kv head for keys (k_scale) and one for values (v_scale).  Element x of
+ *     kv head g is stored as the code nearest to fl32(x / scale[g]), ties to
+ *     an even mantissa, saturated to +-448 (NaN stays NaN); a code c stands
+ *     for value(c) * scale[g].  Attention reads every key and value -- the
+ *     active tokens' own new rows included -- through this encoding, so a
+ *     prompt prefilled in chunks over the FP8 cache gives the same result as
+ *     in one call (a NaN code inside a request's visible keys gives an
+ *     unspecified result).  ("Prefill Processing", Prefix Caching: the KV cache data
+ *     type, e.g. FP8 E4M3, and its quantization scales are part of what the
+ *     cached KV means; the pages fix nothing further, so the format and this
+ *     encoding are the library's.)
  *   - Device pointers must be 16-byte aligned.
  *   - Ownership: the caller allocates and frees every buffer, the workspace
  *     included.  The library never allocates, frees or synchronises; all
@@ -74,6 +90,14 @@ typedef enum {
 } cpa_status;
 
 typedef enum { CPA_DTYPE_FP32 = 0, CPA_DTYPE_BF16 = 1 } cpa_dtype;
+
+/* Representation of the K/V pools (cpa_params.kv_format). */
+typedef enum {
+    CPA_KV_SAME = 0,      /* the pools hold elements of cpa_params.dtype */
+    CPA_KV_FP8_E4M3 = 1   /* the pools hold FP8 E4M3 codes with per-kv-head scales (BF16
+                             dtype; chunked_prefill_attention also needs head_dim 128 and
+                             num_heads_q / num_heads_kv dividing 128, else CPA_ERR_UNSUPPORTED) */
+} cpa_kv_format;
 
 /* flags (cpa_params.flags) */
 #define CPA_FLAG_FUSE_KV_WRITE 0x1u /* attention also writes the new K/V into the pool
@@ -128,13 +152,19 @@ typedef struct {
                                  form), in fp32 and rounded to the element type.  The rotated keys
                                  are what the K/V write stores.  The caller's q and k_new are not
                                  modified: the rotated copies live in the workspace. */
+    int32_t kv_format;        /* cpa_kv_format; CPA_KV_SAME for plain pools */
+    const float *k_scale;     /* CPA_KV_FP8_E4M3 only: device [H_kv], finite and > 0 (the caller's
+                                 guarantee; 4-byte aligned, else CPA_ERR_INVALID_ARG); NULL otherwise */
+    const float *v_scale;     /* likewise for the values */
 } cpa_params;
 
 /* Bytes of device workspace chunked_prefill_attention needs for this batch:
  * the split-KV partials of the requests that are split (rounded up to 256
- * bytes) and, when the batch runs on the tensor-core kernel (BF16 with
+ * bytes), the rotated copies of q and k_new when rope_theta > 0, the FP8
+ * codes of k_new and v_new ([T, H_kv, d] bytes each) with the FP8 cache,
+ * and, when the batch runs on the tensor-core kernel (BF16 with
  * num_heads_q / num_heads_kv dividing 128), 256 bytes for that persistent
- * kernel's work counter.  0 for an empty batch and for a CUDA-core batch
+ * kernel's work counter.  Each part starts on a 256-byte boundary.  0 for an empty batch and for a CUDA-core batch
  * with no split.  Reads only host mirrors.  Returns 0 also when the
  * arguments are invalid; chunked_prefill_attention then reports the error. */
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params);
@@ -142,7 +172,8 @@ size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *
 /* Write the K/V rows of every active token into their pool slots: token i of
  * request r goes to the slot of position cached_seq_len[r] + i
  * ("Prefill Processing", Key Concepts: active tokens write new KV to cache;
- * Attention Metadata: slot_mapping).  A byte-exact copy.  k_new/v_new are
+ * Attention Metadata: slot_mapping).  A byte-exact copy (with the FP8 cache:
+ * the E4M3 codes of the rows, see the conventions above).  k_new/v_new are
  * read, k_cache/v_cache written in place.  Only the slots of active tokens
  * change. */
 cpa_status paged_kv_write(const cpa_batch *batch, const cpa_params *params, const void *k_new,

@@ -150,3 +150,60 @@ def test_workspace_size_counts_rotated_copies(lib):
     rk = 512 * 8 * 128 * 2    # rotated new keys
     # the copies come first (256-byte aligned), the work counter stays last
     assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + rk + plain
+
+
+def _fp8_params(lib, k_scale=0x1000, v_scale=0x1000, **kw):
+    base = dict(num_heads_q=32, num_heads_kv=8, head_dim=128, block_size=16, num_blocks=100, kv_segment_size=1024)
+    base.update(kw)
+    p = lib.Params(**base).c()
+    p.kv_format = lib.KV_FP8_E4M3
+    p.k_scale = k_scale
+    p.v_scale = v_scale
+    return p
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(kv_format=2), "invalid"),
+    (dict(k_scale=None), "invalid"),
+    (dict(v_scale=None), "invalid"),
+    (dict(k_scale=0x1002), "invalid"),     # scales must be 4-byte aligned
+    (dict(dtype=0), "unsupported"),        # FP8 codes of BF16 rows only
+])
+def test_fp8_arguments_checked_before_launch(lib, case, expect):
+    case = dict(case)
+    fmt = case.pop("kv_format", None)
+    p = _fp8_params(lib, **case)
+    if fmt is not None:
+        p.kv_format = fmt
+    b, keep = _cbatch(lib, [10], [5], 4)
+    L = lib.load()
+    want = lib.ERR_INVALID_ARG if expect == "invalid" else lib.ERR_UNSUPPORTED
+    assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0,
+                                       None) == want
+    assert L.paged_kv_write(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, None) == want
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(head_dim=64), dict(num_heads_q=24), dict(flags=0x2)])
+def test_fp8_attention_needs_the_tensor_core_kernel(lib, kw):
+    # d = 64, a query group that does not divide 128 (G = 3), or a forced
+    # CUDA-core kernel: the FP8 cache runs on the tensor-core kernel only
+    p = _fp8_params(lib, **kw)
+    b, keep = _cbatch(lib, [10], [5], 4)
+    L = lib.load()
+    assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0,
+                                       None) == lib.ERR_UNSUPPORTED
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == 0
+
+
+def test_workspace_size_counts_fp8_codes(lib):
+    L = lib.load()
+    b, keep = _cbatch(lib, [8000], [512], 600)
+    plain = L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(lib.Params(32, 8, 128, 16, 10000, 1024).c()))
+    codes = 512 * 8 * 128     # one byte per element of k_new (and again of v_new)
+    p = _fp8_params(lib, num_blocks=10000)
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == plain + 2 * codes
+    # with RoPE the rotated queries come first; rotated keys go straight to codes
+    p.rope_theta = 500000.0
+    rq = 512 * 32 * 128 * 2
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + 2 * codes + plain

@@ -95,12 +95,13 @@ def attention_flops(pairs_total: int, num_heads_q: int, head_dim: int, layers: i
 
 
 def algorithmic_bytes(cached: Sequence[int], new: Sequence[int], num_heads_q: int, num_heads_kv: int,
-                      head_dim: int, elem_bytes: int) -> int:
+                      head_dim: int, elem_bytes: int, kv_elem_bytes: Optional[int] = None) -> int:
     """Bytes the method must move once: cached K and V read once per kv head,
     Q / K_new / V_new read, new K/V written into the pool, output written
-    ("Prefill Optimisation", section 6, per-token KV bytes)."""
+    ("Prefill Optimisation", section 6, per-token KV bytes).  kv_elem_bytes:
+    bytes per pool element (1 for the FP8 cache; default elem_bytes)."""
     T = int(sum(int(n) for n in new))
-    kv_row = 2 * num_heads_kv * head_dim * elem_bytes
+    kv_row = 2 * num_heads_kv * head_dim * (elem_bytes if kv_elem_bytes is None else kv_elem_bytes)
     cached_bytes = sum(int(c) for c in cached) * kv_row
     io = T * (num_heads_q + 2 * num_heads_kv) * head_dim * elem_bytes
     write = T * kv_row
@@ -175,10 +176,10 @@ class Workload:
         sh = self.shape
         return [attention_flops(p, sh.num_heads_q, sh.head_dim) for p in self.pairs_per_step()]
 
-    def bytes_per_step(self) -> List[int]:
+    def bytes_per_step(self, kv_elem_bytes: Optional[int] = None) -> List[int]:
         sh = self.shape
         return [algorithmic_bytes(s.cached_seq_len, s.num_new_tokens, sh.num_heads_q, sh.num_heads_kv,
-                                  sh.head_dim, sh.elem_bytes) for s in self.steps]
+                                  sh.head_dim, sh.elem_bytes, kv_elem_bytes) for s in self.steps]
 
     def materialize(self, device="cpu", sentinel: str = SENTINEL_NAN) -> "Tensors":
         return _materialize(self, torch.device(device), sentinel)
@@ -250,6 +251,38 @@ def _materialize(w: Workload, device: torch.device, sentinel: str) -> Tensors:
         k_cache[b, n_valid:] = fill
         v_cache[b, n_valid:] = fill
     return Tensors(q, k, v, k_cache, v_cache)
+
+
+# ---------------------------------------------------------------------------
+# FP8 cache inputs
+# ---------------------------------------------------------------------------
+
+FP8_MAX = 448.0
+
+
+def fp8_scales(num_heads_kv: int, amax: float = 4.5) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-kv-head key and value scales for N(0,1) data: |x| up to about
+    `amax` maps onto the E4M3 range, a little differently per head (so that a
+    wrong head index shows).  float32 [H_kv] each."""
+    g = np.arange(num_heads_kv, dtype=np.float64)
+    k = (amax / FP8_MAX) * (1.0 + 0.125 * g)
+    v = (amax / FP8_MAX) * (1.0 + 0.0625 * ((g * 5) % num_heads_kv))
+    return k.astype(np.float32), v.astype(np.float32)
+
+
+def fp8_pool_codes(pool: torch.Tensor, scale: np.ndarray, chunk_blocks: int = 2048) -> torch.Tensor:
+    """Input generation for FP8 caches: uint8 codes of a pool
+    [num_blocks, bs, H_kv, d] (NaN sentinels become NaN codes), from torch's
+    own float8_e4m3fn conversion of x / scale clamped to the finite range --
+    a library routine, independent of both the library and the oracle; any
+    valid code pattern would serve as cached contents."""
+    s = torch.as_tensor(np.asarray(scale, dtype=np.float32), device=pool.device)[:, None]
+    out = torch.empty(pool.shape, dtype=torch.uint8, device=pool.device)
+    for b0 in range(0, pool.shape[0], chunk_blocks):
+        b1 = min(pool.shape[0], b0 + chunk_blocks)
+        y = (pool[b0:b1].float() / s).clamp(-FP8_MAX, FP8_MAX)
+        out[b0:b1] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
 
 
 def _block_table(rng: np.random.Generator, needs: Sequence[int], num_blocks: int, extra_cols: int,
