@@ -48,6 +48,7 @@
 // CPA_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -83,19 +84,16 @@ struct TcRoles {
 template <int D, bool F8>
 struct TcCfg {
     static constexpr int kHalves = D / 64;           // 64-element (128 B) column chunks
-    static constexpr int kTileBytes = 128 * D * 2;   // 128 rows of D bf16 (Q, K or V tile)
+    static constexpr int kTileBytes = 128 * D * 2;   // 128 rows of D 16-bit values (Q, K or V tile)
     static constexpr int kHalfBytes = kTileBytes / kHalves;
     static constexpr int kQStages = 2;  // the next unit's Q loads while this one runs
-    // bf16 K / V rings the MMAs read.  With FP8 pools the copies land in
-    // separate rings of code tiles (128 rows x D bytes) that the expansion
-    // warps turn into these.
-    static constexpr int kKStages = F8 ? 2 : (D == 128) ? 3 : 6;
-    static constexpr int kVStages = F8 ? 1 : (D == 128) ? 2 : 5;
+    static constexpr int kKStages = (D == 128) ? 3 : 6;
+    static constexpr int kVStages = (D == 128) ? 2 : 5;
+    // FP8 pools: a K / V copy brings a code tile (128 rows x D bytes) into the
+    // upper half of its ring slot, and the expansion warps turn it in place
+    // into the 16-bit tile the MMAs read
     static constexpr int kCodeTileBytes = 128 * D;
-    static constexpr int kK8Stages = F8 ? 2 : 0;
-    static constexpr int kV8Stages = F8 ? 2 : 0;
-    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages) +
-                                      kCodeTileBytes * (kK8Stages + kV8Stages);
+    static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages);
 };
 
 struct __align__(8) TcShared {
@@ -107,8 +105,7 @@ struct __align__(8) TcShared {
     uint64_t pv_done[kSBuf];  // per score buffer: the PV that read its P has completed
     uint64_t o_full, o_empty;
     uint64_t mma_done;
-    uint64_t k8_full[2], k8_empty[2];  // FP8 pools: code-tile rings
-    uint64_t v8_full[2], v8_empty[2];
+    uint64_t k8_full[6], v8_full[6];  // FP8 pools: a slot's code tile has landed
     // unit scheduler: warp 8 takes unit indices from the launch's work
     // counter and passes them to the other roles through this ring
     uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
@@ -195,63 +192,74 @@ struct TileList {
     }
 };
 
-// Four E4M3 codes (bytes of w, lowest address first) as bf16: element pairs
-// (0, 1) in the first word, (2, 3) in the second, lower column in the low half.
-// From the two formats' layouts: a code s.eeee.mmm placed with its low seven
-// bits at bf16 bits 10..4 and its sign at bit 15 reads as the bf16 number
-// 2^-120 * value (the bf16 exponent bias is 127, the E4M3 one 7, and a code
-// with exponent field 0 lands on a bf16 subnormal with the same m * 2^-9
-// scaled by 2^-120); one exact bf16 multiply by 2^120 restores the value.
-// PRMT builds each 16-bit half as [sign byte | code] (selector nibbles with
-// bit 3 replicate a byte's sign), a shift by 4 moves the code to bits 11..4
-// and the mask keeps the sign and bits 10..4.
-__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));  // [S(b1) b1 S(b0) b0]
-    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));  // [S(b3) b3 S(b2) b2]
-    a = (a << 4) & 0x87F087F0u;
-    b = (b << 4) & 0x87F087F0u;
-    constexpr uint32_t k2p120 = 0x7B807B80u;  // bf16 2^120 in both halves
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(k2p120));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(k2p120));
+// Four E4M3 codes (bytes of w, lowest address first) as fp16 pairs: codes
+// 0, 1 in the first word, 2, 3 in the second, lower column in the low half.
+// Every E4M3 value is an fp16 value (3 mantissa bits; exponents 2^-9 .. 2^8),
+// so the conversion is exact.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const unsigned short a = (unsigned short)(w & 0xffffu), b = (unsigned short)(w >> 16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(a));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(b));
 }
 
-// Rows [r0, r0 + 64) of one 128 x 128 code tile (rows of 128 bytes) into the
-// bf16 tile the MMAs read: two 64-column halves of 128 rows x 128 B, 16-byte
-// chunk c of row r at chunk position c ^ (r % 8) (the 128-byte swizzle).
-// Rows at or past `valid` are written as zeros when zero_tail is set, else
-// left as they are.  Eight lanes share a row: lane piece p (16 codes, columns
-// 16p .. 16p + 15) fills chunks 2(p % 4) and 2(p % 4) + 1 of half p / 4.
-// Which of its two chunks a lane handles first alternates with the half and
-// with the row's parity: then every store instruction covers all eight chunk
-// positions of each row, and every 8-byte load instruction reads row pairs
-// whose byte ranges fall on complementary banks -- neither conflicts.
-__device__ __forceinline__ void expand_code_rows(const uint8_t *src, uint8_t *dst, int r0, int valid, bool zero_tail,
-                                                 int lane, int half_bytes) {
+// Rows [r0, r0 + 64) of a 128 x 128 code tile, held in the upper half of its
+// ring slot (rows of 128 bytes at slot + 16 KB), expanded in place into the
+// 16-bit tile the MMAs read: two 64-column halves of 128 rows x 128 B at
+// slot and slot + 16 KB, 16-byte chunk c of row r at chunk position
+// c ^ (r % 8) (the 128-byte swizzle).  Half 1 of row r overwrites code row r
+// only, so reading each row before writing it keeps the expansion in place;
+// a batch of eight rows per lane is read before any of them is written (the
+// loads then overlap), and the two warps of a tile own disjoint rows.
+// Rows at or past `valid` become zeros when zero_tail is set (code 0), else
+// they are left as they are.  Eight lanes share a row: lane piece p (16
+// codes, columns 16p .. 16p + 15) fills chunks 2(p % 4) and 2(p % 4) + 1 of
+// half p / 4.  Which of its two chunks a lane handles first alternates with
+// the half and with the row's parity: then every store instruction covers all
+// eight chunk positions of each row, and every 8-byte load instruction reads
+// row pairs whose byte ranges fall on complementary banks -- neither
+// conflicts.
+__device__ __forceinline__ void expand_code_rows(uint8_t *slot, int r0, int valid, bool zero_tail, int lane,
+                                                 int half_bytes) {
+    const uint8_t *codes = slot + half_bytes;
     const int p = lane & 7;
     const int h = p >> 2;
     const int f = h ^ ((lane >> 3) & 1);  // r0 is even, so (lane >> 3) & 1 is the row's parity
     const int c_first = 2 * (p & 3) + f, c_second = 2 * (p & 3) + 1 - f;
-#pragma unroll 4
-    for (int it = 0; it < 16; ++it) {
-        const int r = r0 + it * 4 + (lane >> 3);
-        uint8_t *row = dst + h * half_bytes + r * 128;
-        const int sw = r & 7;
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-        if (r < valid) {
-            const uint8_t *in = src + r * 128 + p * 16;
-            const uint2 w0 = *reinterpret_cast<const uint2 *>(in + 8 * f);        // codes of chunk c_first
-            const uint2 w1 = *reinterpret_cast<const uint2 *>(in + 8 * (1 - f));  // codes of chunk c_second
-            e4m3x4_to_bf16(w0.x, o0.x, o0.y);
-            e4m3x4_to_bf16(w0.y, o0.z, o0.w);
-            e4m3x4_to_bf16(w1.x, o1.x, o1.y);
-            e4m3x4_to_bf16(w1.y, o1.z, o1.w);
-        } else if (!zero_tail) {
-            continue;
+    constexpr int kBatch = 8;
+#pragma unroll 1
+    for (int it0 = 0; it0 < 16; it0 += kBatch) {
+        uint2 w0[kBatch], w1[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int r = r0 + (it0 + i) * 4 + (lane >> 3);
+            w0[i] = make_uint2(0, 0);
+            w1[i] = make_uint2(0, 0);
+            if (r < valid) {
+                const uint8_t *in = codes + r * 128 + p * 16;
+                w0[i] = *reinterpret_cast<const uint2 *>(in + 8 * f);        // codes of chunk c_first
+                w1[i] = *reinterpret_cast<const uint2 *>(in + 8 * (1 - f));  // codes of chunk c_second
+            }
         }
-        *reinterpret_cast<uint4 *>(row + ((c_first ^ sw) << 4)) = o0;
-        *reinterpret_cast<uint4 *>(row + ((c_second ^ sw) << 4)) = o1;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int r = r0 + (it0 + i) * 4 + (lane >> 3);
+            if (r >= valid && !zero_tail) continue;
+            uint4 o0, o1;
+            e4m3x4_to_f16(w0[i].x, o0.x, o0.y);
+            e4m3x4_to_f16(w0[i].y, o0.z, o0.w);
+            e4m3x4_to_f16(w1[i].x, o1.x, o1.y);
+            e4m3x4_to_f16(w1[i].y, o1.z, o1.w);
+            uint8_t *row = slot + h * half_bytes + r * 128;
+            const int sw = r & 7;
+            *reinterpret_cast<uint4 *>(row + ((c_first ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4 *>(row + ((c_second ^ sw) << 4)) = o1;
+        }
     }
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // The i-th unit of this CTA, as published by the scheduling warp (every lane
@@ -286,8 +294,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     uint8_t *sQ = smem;                // 2 stages
     uint8_t *sK = smem + Cfg::kQStages * TB;  // NSK stages
     uint8_t *sV = sK + NSK * TB;       // NSV stages
-    uint8_t *sK8 = sV + NSV * TB;      // FP8 pools: code tiles of K, then of V
-    uint8_t *sV8 = sK8 + Cfg::kK8Stages * CB;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -297,26 +303,21 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     const int end_index = total_units + a.write_chunks;  // then the fused K/V write
 
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < Cfg::kQStages; ++b) {
             mbar_init(&sh.q_full[b], 1);
             mbar_init(&sh.q_empty[b], 1);
         }
-        // bf16 tiles: filled by one TMA arrival, or by the two expansion warps
+        // 16-bit tiles: filled by one TMA arrival, or (FP8 pools) by the two
+        // expansion warps once the code tile's copies (k8 / v8_full) landed
         for (int s = 0; s < NSK; ++s) {
             mbar_init(&sh.k_full[s], F8 ? 2 : 1);
             mbar_init(&sh.k_empty[s], 1);
+            mbar_init(&sh.k8_full[s], 1);
         }
         for (int s = 0; s < NSV; ++s) {
             mbar_init(&sh.v_full[s], F8 ? 2 : 1);
             mbar_init(&sh.v_empty[s], 1);
-        }
-        for (int s = 0; s < Cfg::kK8Stages; ++s) {
-            mbar_init(&sh.k8_full[s], 1);
-            mbar_init(&sh.k8_empty[s], 2);
-        }
-        for (int s = 0; s < Cfg::kV8Stages; ++s) {
             mbar_init(&sh.v8_full[s], 1);
-            mbar_init(&sh.v8_empty[s], 2);
         }
         for (int b = 0; b < kSBuf; ++b) {
             mbar_init(&sh.s_full[b], 1);
@@ -354,11 +355,12 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // ================================================================ TMA
         const int kv_role = (warp == kVProducerWarp) ? 1 : 0;  // copies K (0) or V (1)
         bool ok = true;
-        // ring the copies go to: the bf16 tiles, or with FP8 pools the code tiles
-        const int ns = F8 ? (kv_role ? Cfg::kV8Stages : Cfg::kK8Stages) : (kv_role ? NSV : NSK);
+        // the copies' ring; with FP8 pools a code tile goes to the upper half
+        // of its slot and its own barrier (the expansion then fills the slot)
+        const int ns = kv_role ? NSV : NSK;
         uint64_t *const ring_full = F8 ? (kv_role ? sh.v8_full : sh.k8_full) : (kv_role ? sh.v_full : sh.k_full);
-        uint64_t *const ring_empty = F8 ? (kv_role ? sh.v8_empty : sh.k8_empty) : (kv_role ? sh.v_empty : sh.k_empty);
-        uint8_t *const ring = F8 ? (kv_role ? sV8 : sK8) : (kv_role ? sV : sK);
+        uint64_t *const ring_empty = kv_role ? sh.v_empty : sh.k_empty;
+        uint8_t *const ring = (kv_role ? sV : sK) + (F8 ? HB : 0);
         constexpr int slot_bytes = F8 ? CB : TB;
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             auto load_kv = [&](int j, int kv) -> bool {
                 uint64_t *empty = &ring_empty[slot];
                 uint64_t *full = &ring_full[slot];
-                uint8_t *dst = ring + slot * slot_bytes;
+                uint8_t *dst = ring + slot * TB;
                 if (!__all_sync(0xffffffffu, mbar_wait_or_abort(empty, ph ^ 1u, LIM, abort_flag))) return false;
                 int key0, valid;
                 bool pooled;
@@ -471,11 +473,12 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 // the first K tile does not depend on the Q buffer: issue it
                 // before waiting for the previous unit's last score MMA
                 ok = load_kv(0, 0);
-                // Q stage it % 2; its previous use (unit it - 2) must have
-                // finished its last score MMA
-                const int qb = it & 1;
-                if (ok && it >= 2 &&
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[qb], (uint32_t)(((it - 2) >> 1) & 1), LIM,
+                // Q stage it % kQStages; its previous use (unit it - kQStages)
+                // must have finished its last score MMA
+                constexpr int QS = Cfg::kQStages;
+                const int qb = it % QS;
+                if (ok && it >= QS &&
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[qb], (uint32_t)(((it - QS) / QS) & 1), LIM,
                                                                 abort_flag)))
                     ok = false;
                 if (ok) {
@@ -520,8 +523,10 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         uint32_t rph = 0;            // and the parity of its fill
         long long issued = 0;        // tiles issued by this warp
         bool ok = true;
-        constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+        // bf16 operands; fp16 with FP8 pools (queries scaled per row, codes
+        // expanded exactly, probabilities rounded to fp16)
+        constexpr uint32_t idesc_s = idesc_16bit_f32(128, kKT, 0, 0, !F8);
+        constexpr uint32_t idesc_pv = idesc_16bit_f32(128, D, 0, 1, !F8);
         // Shared-memory descriptors: the high halves (stride, version,
         // swizzle) are common to Q, K and V; only the low halves (start
         // address >> 4 and leading byte offset) differ.  Addresses stay below
@@ -549,9 +554,9 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             const int n = tl.n_total;
             if (s_role) {
                 // S(j) = Q K(j)^T, as far ahead as the score buffers allow
-                const int qb = ucnt & 1;
+                const int qb = ucnt % Cfg::kQStages;
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&sh.q_full[qb], (uint32_t)((ucnt >> 1) & 1), LIM, abort_flag))) {
+                                mbar_wait_or_abort(&sh.q_full[qb], (uint32_t)((ucnt / Cfg::kQStages) & 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -654,16 +659,16 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         __syncwarp();
     } else if (F8 && warp >= kKConvWarp) {
         // ==================================== FP8 expansion (warps 12-15)
-        // Warps 12-13 turn K code tiles into bf16 K tiles, 14-15 V tiles; each
-        // warp takes 64 rows.  V rows past a tile's valid keys become zeros
-        // (P = 0 must not meet a NaN code left in the pool or the ring); K
-        // rows there are left as they are, the softmax masks their scores.
+        // Warps 12-13 expand K code tiles, 14-15 V tiles, in their ring slots;
+        // each warp takes 64 rows.  V rows past a tile's valid keys become
+        // zeros (P = 0 must not meet a NaN code left in the pool or a stale
+        // value); K rows there are left as they are, the softmax masks their
+        // scores.
         const int kv = (warp - kKConvWarp) >> 1;
         const int r0 = ((warp - kKConvWarp) & 1) * 64;
-        const int ns8 = kv ? Cfg::kV8Stages : Cfg::kK8Stages;
         const int nsb = kv ? NSV : NSK;
-        int s8 = 0, sb = 0;
-        uint32_t ph8 = 0, phb = 0;
+        int sb = 0;
+        uint32_t phb = 0;
         bool ok = true;
         for (int cc = 0;; ++cc) {
             const int unit = read_unit(sh, cc, LIM, abort_flag);
@@ -679,29 +684,19 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             TileList tl;
             tl.init(u);
             for (int j = 0; j < tl.n_total; ++j) {
-                uint64_t *code_full = kv ? &sh.v8_full[s8] : &sh.k8_full[s8];
-                uint64_t *code_empty = kv ? &sh.v8_empty[s8] : &sh.k8_empty[s8];
-                uint64_t *bf_full = kv ? &sh.v_full[sb] : &sh.k_full[sb];
-                uint64_t *bf_empty = kv ? &sh.v_empty[sb] : &sh.k_empty[sb];
-                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bf_empty, phb ^ 1u, LIM, abort_flag)) ||
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(code_full, ph8, LIM, abort_flag))) {
+                uint64_t *code_full = kv ? &sh.v8_full[sb] : &sh.k8_full[sb];
+                uint64_t *tile_full = kv ? &sh.v_full[sb] : &sh.k_full[sb];
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(code_full, phb, LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
                 int key0, valid;
                 bool pooled;
                 tl.tile(j, key0, valid, pooled);
-                expand_code_rows((kv ? sV8 : sK8) + s8 * CB, (kv ? sV : sK) + sb * TB, r0, valid, kv == 1, lane, HB);
+                expand_code_rows((kv ? sV : sK) + sb * TB, r0, valid, kv == 1, lane, HB);
                 fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bf_full);
-                    mbar_arrive(code_empty);
-                }
-                if (++s8 == ns8) {
-                    s8 = 0;
-                    ph8 ^= 1u;
-                }
+                if (lane == 0) mbar_arrive(tile_full);
                 if (++sb == nsb) {
                     sb = 0;
                     phb ^= 1u;
@@ -752,11 +747,15 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             const int n = tl.n_total;
             const bool row_valid = lr < u.rows;
             const int pos = row_valid ? u.C + (u.row0 + lr) / a.G : -1;
-            // FP8 pools: the tiles hold code values; a key's scale multiplies
-            // every score of the unit (one kv head), a value's scale the output
+            // FP8 pools: the tiles hold code values and the queries were
+            // scaled by a power of two per row; the key scale and the row's
+            // inverse query scale multiply its scores, the value scale the output
             float v_mul = 1.f;
             if (F8) {
-                sl = a.scale_log2 * __ldg(a.k_scale + u.g);
+                const int pr = u.row0 + lr;
+                const float q_mul =
+                    row_valid ? __ldg(a.q_rscale + (long long)(u.cu0 + pr / a.G) * a.hq + u.g * a.G + pr % a.G) : 1.f;
+                sl = a.scale_log2 * __ldg(a.k_scale + u.g) * q_mul;
                 v_mul = __ldg(a.v_scale + u.g);
             }
             float m_ref = -INFINITY, l = 0.f;
@@ -845,7 +844,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                             acc1 = __fadd2_rn(acc1, e);
                         else
                             acc0 = __fadd2_rn(acc0, e);
-                        r[i] = pack_bf16(e.x, e.y);
+                        r[i] = F8 ? pack_f16(e.x, e.y) : pack_bf16(e.x, e.y);
                     }
                     tmem_st16x2_32<32>(tS, r);  // threads 0-15: P columns 0-31, 16-31: 32-63
                 }

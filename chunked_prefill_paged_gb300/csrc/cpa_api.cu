@@ -125,6 +125,7 @@ struct Plan {
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
     size_t rq_off = 0, rk_off = 0;  // rotated q / k_new copies (rope_theta > 0)
     size_t kq_off = 0, vq_off = 0;  // FP8 cache: codes of k_new / v_new
+    size_t q16_off = 0, qs_off = 0; // FP8 cache: fp16 queries and their row scales
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
     int direct_units = 0;
@@ -170,15 +171,17 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
         pl.ws_bytes = off + bytes;
         return off;
     };
-    if (p->rope_theta > 0.f) {
-        // rotated copies of q and (plain pools) k_new, which the attention then reads
-        pl.rq_off = take(T * p->num_heads_q * d * es);
-        if (!kv_fp8(p)) pl.rk_off = take(T * p->num_heads_kv * d * es);
-    }
     if (kv_fp8(p)) {
-        // the new rows as the FP8 cache holds them, read by the attention
+        // the (rotated) queries as fp16 with their row scales, and the new rows
+        // as the FP8 cache holds them, which the attention then reads
+        pl.q16_off = take(T * p->num_heads_q * d * 2);
+        pl.qs_off = take(T * p->num_heads_q * sizeof(float));
         pl.kq_off = take(T * p->num_heads_kv * d);
         pl.vq_off = take(T * p->num_heads_kv * d);
+    } else if (p->rope_theta > 0.f) {
+        // rotated copies of q and k_new, which the attention then reads
+        pl.rq_off = take(T * p->num_heads_q * d * es);
+        pl.rk_off = take(T * p->num_heads_kv * d * es);
     }
     if (tc) {
         // the persistent kernel's work counter, after the partials
@@ -189,14 +192,20 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
 }
 
 
-// bf16 tiles land 128-byte swizzled (the MMA operand layout); FP8 code tiles
-// land as plain rows for the expansion warps
+// 16-bit tiles land 128-byte swizzled (the MMA operand layout); FP8 code
+// tiles land as plain rows for the expansion warps
+enum class MapType { kBf16, kF16, kCodes };
+
 cpa_status encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                  const cuuint32_t *box, bool codes = false) {
+                  const cuuint32_t *box, MapType type = MapType::kBf16) {
     auto enc = tensor_map_encoder();
     if (!enc) return CPA_ERR_CUDA;
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+    const bool codes = type == MapType::kCodes;
+    const CUtensorMapDataType dt = codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : type == MapType::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = enc(map, dt, (cuuint32_t)rank,
                      const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -212,7 +221,9 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
         const cuuint64_t dims[3] = {D, Hq, T};
         const cuuint64_t strides[2] = {D * 2, Hq * D * 2};
         const cuuint32_t box[3] = {64, G, (cuuint32_t)kTcTileM / G};
-        if (cpa_status s = encode(&m.q, q, 3, dims, strides, box)) return s;
+        // with the FP8 cache q is the pre-pass's fp16 copy
+        if (cpa_status s = encode(&m.q, q, 3, dims, strides, box, kv_fp8(p) ? MapType::kF16 : MapType::kBf16))
+            return s;
     }
     const cuuint32_t box_rows = (cuuint32_t)(bs < (cuuint64_t)kTcTileN ? bs : (cuuint64_t)kTcTileN);
     if (kv_fp8(p)) {
@@ -220,13 +231,13 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
         const cuuint64_t dims3[3] = {D, Hkv, T};
         const cuuint64_t strides3[2] = {D, Hkv * D};
         const cuuint32_t box3[3] = {(cuuint32_t)D, 1, (cuuint32_t)kTcTileN};
-        if (cpa_status s = encode(&m.k_new, k_new, 3, dims3, strides3, box3, true)) return s;
-        if (cpa_status s = encode(&m.v_new, v_new, 3, dims3, strides3, box3, true)) return s;
+        if (cpa_status s = encode(&m.k_new, k_new, 3, dims3, strides3, box3, MapType::kCodes)) return s;
+        if (cpa_status s = encode(&m.v_new, v_new, 3, dims3, strides3, box3, MapType::kCodes)) return s;
         const cuuint64_t dims4[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
         const cuuint64_t strides4[3] = {D, Hkv * D, bs * Hkv * D};
         const cuuint32_t box4[4] = {(cuuint32_t)D, 1, box_rows, 1};
-        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims4, strides4, box4, true)) return s;
-        return encode(&m.v_pool, v_cache, 4, dims4, strides4, box4, true);
+        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims4, strides4, box4, MapType::kCodes)) return s;
+        return encode(&m.v_pool, v_cache, 4, dims4, strides4, box4, MapType::kCodes);
     }
     {
         const cuuint64_t dims[3] = {D, Hkv, T};
@@ -357,6 +368,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     if (cpa_status s = device_info(dev)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
+    const float *q_rscale = nullptr;
     if (params->rope_theta > 0.f || kv_fp8(params)) {
         // pre-pass over the new rows: rotate q and k_new, encode the keys and
         // values for the FP8 cache, into workspace copies that the attention
@@ -367,10 +379,12 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         r.q = q;
         r.k_new = k_new;
         r.v_new = v_new;
-        r.q_rot = r.rotate ? ws + pl.rq_off : nullptr;
+        r.q_rot = (r.rotate && !r.kv_fp8) ? ws + pl.rq_off : nullptr;
         r.k_rot = (r.rotate && !r.kv_fp8) ? ws + pl.rk_off : nullptr;
         r.k_q8 = r.kv_fp8 ? ws + pl.kq_off : nullptr;
         r.v_q8 = r.kv_fp8 ? ws + pl.vq_off : nullptr;
+        r.q16 = r.kv_fp8 ? ws + pl.q16_off : nullptr;
+        r.q_rscale = r.kv_fp8 ? reinterpret_cast<float *>(ws + pl.qs_off) : nullptr;
         r.write_pool = fuse_write ? 1 : 0;
         r.k_cache = k_cache;
         r.v_cache = v_cache;
@@ -378,8 +392,10 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         if (r.q_rot) q = r.q_rot;
         if (r.k_rot) k_new = r.k_rot;
         if (r.kv_fp8) {
+            q = r.q16;
             k_new = r.k_q8;
             v_new = r.v_q8;
+            q_rscale = r.q_rscale;
         }
         fuse_write = false;
     }
@@ -430,6 +446,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.kv_fp8 = kv_fp8(params) ? 1 : 0;
     a.k_scale = params->k_scale;
     a.v_scale = params->v_scale;
+    a.q_rscale = q_rscale;
 
     cudaError_t e;
     if (pl.tile_m == kTcTileM) {

@@ -116,10 +116,12 @@ struct AttnArgs {
     long long timeout_cycles;
     int test_stall;     // testing only: withhold the first K tile's copies
     // FP8 cache: pools and k_new / v_new (the workspace copies of the new rows'
-    // codes) hold E4M3 codes; a code of kv head g stands for value * scale[g]
+    // codes) hold E4M3 codes; a code of kv head g stands for value * scale[g].
+    // q is then fp16, row (t, h) scaled by 2^e; q_rscale[t * hq + h] = 2^-e.
     int kv_fp8;
     const float *k_scale;  // [hkv]
     const float *v_scale;  // [hkv]
+    const float *q_rscale; // [T, hq]
 };
 
 // Arguments of the pre-pass over the active tokens' rows: with rotate, turns
@@ -153,6 +155,8 @@ struct RopeArgs {
     const float *v_scale; // [hkv]
     void *k_q8;           // [T, hkv, d] codes of the keys, or null
     void *v_q8;           // [T, hkv, d] codes of the values, or null
+    void *q16;            // [T, hq, d] fp16 queries (FP8-cache attention), or null
+    float *q_rscale;      // [T, hq] inverse power-of-two scale of each q16 row
 };
 
 // Arguments of the standalone KV write.

@@ -10,6 +10,7 @@
 // carried across key tiles (online softmax), in the log2 domain: scores are
 // multiplied by scale * log2(e) and exponentiated with exp2.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -52,7 +53,12 @@ cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stre
 // FP8 cache: each key (after rotation, as the element type) and value
 // element x of kv head g becomes the E4M3 code of fl32(x / scale[g]) --
 // correctly rounded division, then the hardware conversion, round to
-// nearest even with saturation to +-448.
+// nearest even with saturation to +-448.  The attention over FP8 pools runs
+// its MMAs in fp16, so each query row (after rotation, as the element type)
+// is also written as fp16 times 2^e, e chosen so that the row's largest
+// magnitude lands in [2^14, 2^15): every element within 2^-28 of that
+// maximum converts exactly (bf16 keeps 8 significant bits, fp16 11), and
+// 2^-e goes to q_rscale for the softmax to undo.
 //
 // Lane l owns pairs c = 2l, 2l + 1 (d = 128) or c = l (d = 64), so the warp's
 // accesses to each half row are contiguous.
@@ -89,7 +95,7 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     for (int c = threadIdx.x; c < HALF; c += blockDim.x) frac_s[c] = a.turn_frac[c];
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int head_lo = a.q_rot ? 0 : a.hq;  // without rotated queries only key heads
+    const int head_lo = (a.q_rot || a.q16) ? 0 : a.hq;  // key heads only unless queries are written
     const int heads = a.hq + a.hkv;
     const int groups = (heads - head_lo + kHeadsPerWarp - 1) / kHeadsPerWarp;
     const long long wid = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -133,6 +139,32 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
                 xl.e[e] = from_float<T>(x0 * cs[e] - x1 * sn[e]);
                 xh.e[e] = from_float<T>(x1 * cs[e] + x0 * sn[e]);
             }
+        }
+        if (is_q && a.q16) {
+            // fp16 copy scaled by 2^e per row (see above)
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < PPL; ++e) amax = fmaxf(amax, fmaxf(fabsf(to_float(xl.e[e])), fabsf(to_float(xh.e[e]))));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            int ex = 0;
+            if (amax > 0.f) frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+            const int e = max(-100, min(100, amax > 0.f ? 15 - ex : 0));
+            const float up = __int_as_float((127 + e) << 23), down = __int_as_float((127 - e) << 23);
+            union {
+                typename LaneVec<PPL * 2>::type v;
+                __half e[PPL];
+            } q_lo, q_hi;
+#pragma unroll
+            for (int e2 = 0; e2 < PPL; ++e2) {
+                q_lo.e[e2] = __float2half_rn(to_float(xl.e[e2]) * up);
+                q_hi.e[e2] = __float2half_rn(to_float(xh.e[e2]) * up);
+            }
+            __half *dst = static_cast<__half *>(a.q16) + row;
+            *reinterpret_cast<typename LaneVec<PPL * 2>::type *>(dst + lane * PPL) = q_lo.v;
+            *reinterpret_cast<typename LaneVec<PPL * 2>::type *>(dst + HALF + lane * PPL) = q_hi.v;
+            if (lane == 0) a.q_rscale[(long long)t * a.hq + hh] = down;
+            continue;
         }
         if (is_q) {
             T *dst = static_cast<T *>(a.q_rot) + row;
@@ -183,7 +215,7 @@ cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (a.total_tokens == 0) return cudaSuccess;
     const int warps = 8;
-    const int heads = a.q_rot ? a.hq + a.hkv : a.hkv;
+    const int heads = (a.q_rot || a.q16) ? a.hq + a.hkv : a.hkv;
     const long long work = (long long)a.total_tokens * ((heads + kHeadsPerWarp - 1) / kHeadsPerWarp);
     const int blocks = (int)((work + warps - 1) / warps);
     if (a.elem_bytes == 2) {

@@ -310,14 +310,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // Instruction descriptor, .kind::f16 with bf16 inputs and f32 accumulate.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+// kind::f16 with fp32 accumulation; A and B both bf16 (bf16 = true) or both
+// fp16 (bf16 = false)
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N, int a_mn, int b_mn, bool bf16) {
     return (1u << 4)                      // D format: f32
-           | (1u << 7)                    // A format: bf16
-           | (1u << 10)                   // B format: bf16
+           | ((bf16 ? 1u : 0u) << 7)      // A format: bf16 (1) or f16 (0)
+           | ((bf16 ? 1u : 0u) << 10)     // B format: likewise
            | ((uint32_t)a_mn << 15)       // A major
            | ((uint32_t)b_mn << 16)       // B major
            | ((uint32_t)(N >> 3) << 17)   // N / 8
            | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+    return idesc_16bit_f32(M, N, a_mn, b_mn, true);
 }
 
 }  // namespace ptx

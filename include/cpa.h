@@ -51,7 +51,10 @@
  *     active tokens' own new rows included -- through this encoding, so a
  *     prompt prefilled in chunks over the FP8 cache gives the same result as
  *     in one call (a NaN code inside a request's visible keys gives an
- *     unspecified result).  ("Prefill Processing", Prefix Caching: the KV cache data
+ *     unspecified result).  The attention then multiplies in fp16: each query
+ *     row is scaled by a power of two that puts its largest magnitude in
+ *     [2^14, 2^15) (exact for every element within 2^-28 of that maximum)
+ *     and the probabilities are rounded to fp16 (finer than bf16).  ("Prefill Processing", Prefix Caching: the KV cache data
  *     type, e.g. FP8 E4M3, and its quantization scales are part of what the
  *     cached KV means; the pages fix nothing further, so the format and this
  *     encoding are the library's.)
@@ -160,8 +163,10 @@ typedef struct {
 
 /* Bytes of device workspace chunked_prefill_attention needs for this batch:
  * the split-KV partials of the requests that are split (rounded up to 256
- * bytes), the rotated copies of q and k_new when rope_theta > 0, the FP8
- * codes of k_new and v_new ([T, H_kv, d] bytes each) with the FP8 cache,
+ * bytes), the rotated copies of q and k_new when rope_theta > 0 (plain
+ * pools), with the FP8 cache the fp16 copy of q ([T, H_q, d] x 2 bytes), its
+ * row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new ([T, H_kv,
+ * d] bytes each),
  * and, when the batch runs on the tensor-core kernel (BF16 with
  * num_heads_q / num_heads_kv dividing 128), 256 bytes for that persistent
  * kernel's work counter.  Each part starts on a 256-byte boundary.  0 for an empty batch and for a CUDA-core batch

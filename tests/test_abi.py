@@ -200,10 +200,11 @@ def test_workspace_size_counts_fp8_codes(lib):
     L = lib.load()
     b, keep = _cbatch(lib, [8000], [512], 600)
     plain = L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(lib.Params(32, 8, 128, 16, 10000, 1024).c()))
+    q16 = 512 * 32 * 128 * 2  # fp16 queries
+    qs = 512 * 32 * 4         # their row scales
     codes = 512 * 8 * 128     # one byte per element of k_new (and again of v_new)
     p = _fp8_params(lib, num_blocks=10000)
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == plain + 2 * codes
-    # with RoPE the rotated queries come first; rotated keys go straight to codes
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == q16 + qs + 2 * codes + plain
+    # with RoPE the rotation goes straight into those copies
     p.rope_theta = 500000.0
-    rq = 512 * 32 * 128 * 2
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + 2 * codes + plain
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == q16 + qs + 2 * codes + plain
