@@ -150,6 +150,18 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     pl.tiles_per_unit = 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     const int G = p->num_heads_q / p->num_heads_kv;
+    // fewer, longer split units while the batch keeps enough of them: every
+    // unit costs a switch (its lookups, the epilogue, the pipeline's refill)
+    for (int len = pl.split_len * 2; pl.split_len > 0 && len <= kMaxSplitLen; len *= 2) {
+        long long units = 0;
+        for (int r = 0; r < b->num_reqs; ++r) {
+            const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
+                                           p->head_dim, pl.tile_m, len, pl.tiles_per_unit);
+            units += w.direct_units + w.split_units;
+        }
+        if (units < kSplitTargetUnits) break;
+        pl.split_len = len;
+    }
     double kv_bytes = 0;
     for (int r = 0; r < b->num_reqs; ++r) {
         const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,

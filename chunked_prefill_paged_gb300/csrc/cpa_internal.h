@@ -32,6 +32,12 @@ constexpr int kTcTileM = 128;    // packed query rows per tensor-core tile
 constexpr int kTcTileN = 128;    // keys per K/V tile of the tensor-core kernel
 constexpr int kSimtTileM = 16;   // packed query rows per CUDA-core tile
 constexpr int kDefaultSplit = 1024;
+// A CTA takes several consecutive kv_segment_size pieces of a decode's keys
+// (carried by its online softmax) while the batch still has at least this
+// many units -- about seven per SM on a 152-SM GB300, enough for the dynamic
+// scheduler to balance -- up to kMaxSplitLen keys per unit.
+constexpr int kSplitTargetUnits = 1024;
+constexpr int kMaxSplitLen = 8192;
 // 16-byte pieces of the new K/V rows per fused-write chunk of the tensor-core
 // kernel (each piece index copies 16 bytes of K and 16 bytes of V)
 constexpr int kWriteChunkPieces = 1024;

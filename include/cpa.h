@@ -138,9 +138,12 @@ typedef struct {
     int32_t block_size;       /* tokens per cache block: 16, 32, 64 or 128 */
     int32_t num_blocks;       /* blocks in each pool */
     int32_t kv_segment_size;  /* 0 (library chooses) or 512, 1024, 2048, 4096; a multiple of
-                                 block_size ("Prefill Processing", Kernel Interface).  It is the
-                                 unit in which the keys of single-tile requests (decodes) are
-                                 split across CTAs and merged. */
+                                 block_size ("Prefill Processing", Kernel Interface).  The keys
+                                 of single-tile requests (decodes) are walked in pieces of this
+                                 size, combined by online-softmax merging.  When the batch has
+                                 plenty of work a CTA takes 2, 4 or 8 consecutive pieces (up to
+                                 8192 keys, while at least 1024 units remain); the result is the
+                                 same up to rounding. */
     float scale;              /* softmax scale applied to q.k, finite and > 0 (usually 1/sqrt(d)) */
     int32_t dtype;            /* cpa_dtype */
     uint32_t flags;           /* CPA_FLAG_* */
