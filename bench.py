@@ -10,7 +10,9 @@ Printed (rank 0, one JSON line): algorithmic attention TFLOP/s =
 4 * H_q * d * visible pairs / time, with the roofline of the attention
 kernel, the end-to-end number through the Python API with host buffers, the
 oracle timed on the host cores, the SM clocks seen during the timed region,
-and a secondary line for the decode-heavy mixed step (KV-read GB/s).
+a secondary line for the decode-heavy mixed step (KV-read GB/s), and the
+same mixed step over an FP8 (E4M3) cache ("fp8_mixed", pool bytes counted
+at one per element).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
   python bench.py --case NAME [--steps K --warmup W]
@@ -24,6 +26,7 @@ under ncu and per-configuration timing) and prints {"case": ..., "ms": ...}:
   mixed_step         64 decodes + 512-token chunks under a 2048 budget
   prefix_cache       16 requests sharing a 4096-token cached prefix
   speculative_decode 64 requests x 5 tokens (1 + 4 drafts) over contexts U{1024..32768}
+  *_fp8              mixed_step, llama_chunk, speculative_decode over FP8 (E4M3) pools
 """
 from __future__ import annotations
 
@@ -51,15 +54,30 @@ METRIC = "chunk-attn TFLOP/s (algorithmic, visible pairs only)"
 UNIT = "TFLOP/s"
 
 
-# name -> (workload constructor, step index, rope_theta)
+# name -> (workload constructor, step index, rope_theta, FP8 pools)
 CASES = {
-    "llama_chunk": (W.llama3_8b_prompt, -1, 0.0),
-    "llama_chunk_rope": (W.llama3_8b_prompt, -1, 500000.0),
-    "long_context_last": (W.long_context, -1, 0.0),
-    "mixed_step": (W.mixed_step, 0, 0.0),
-    "prefix_cache": (W.prefix_cache, 0, 0.0),
-    "speculative_decode": (W.speculative_decode, 0, 0.0),
+    "llama_chunk": (W.llama3_8b_prompt, -1, 0.0, False),
+    "llama_chunk_rope": (W.llama3_8b_prompt, -1, 500000.0, False),
+    "long_context_last": (W.long_context, -1, 0.0, False),
+    "mixed_step": (W.mixed_step, 0, 0.0, False),
+    "prefix_cache": (W.prefix_cache, 0, 0.0, False),
+    "speculative_decode": (W.speculative_decode, 0, 0.0, False),
+    "llama_chunk_fp8": (W.llama3_8b_prompt, -1, 0.0, True),
+    "mixed_step_fp8": (W.mixed_step, 0, 0.0, True),
+    "speculative_decode_fp8": (W.speculative_decode, 0, 0.0, True),
 }
+
+
+def fp8_inputs(cpa, w, t, params, dev):
+    """Turn a materialized workload's pools into FP8 codes (input
+    generation by torch's float8 conversion) and point params at them."""
+    ks, vs = W.fp8_scales(w.shape.num_heads_kv)
+    k8 = W.fp8_pool_codes(t.k_cache, ks)
+    v8 = W.fp8_pool_codes(t.v_cache, vs)
+    t.k_cache, t.v_cache = k8, v8
+    params.kv_format = cpa.KV_FP8_E4M3
+    params.k_scale = torch.as_tensor(ks, device=dev)
+    params.v_scale = torch.as_tensor(vs, device=dev)
 
 
 def parse_args():
@@ -322,12 +340,13 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
                 "traffic": rec["bytes_per_launch"] if rec else None,
-                "kernel": "attn_tc_kernel<128>",
+                "kernel": "attn_tc_kernel<128, false>",
                 "algorithmic_flops_per_launch": flops_step / len(w.steps)}
 
-    secondary = None
+    secondary = fp8_mixed = None
     if not args.no_secondary:
         secondary = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush)
+        fp8_mixed = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=True)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -351,12 +370,14 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "cpu_baseline": cpu,
         "secondary": secondary,
+        "fp8_mixed": fp8_mixed,
     }
     return line
 
 
-def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush):
-    """Decode-heavy mixed step (64 decodes + 4 prefill chunks): KV-read GB/s."""
+def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=False):
+    """Decode-heavy mixed step (64 decodes + 4 prefill chunks): KV-read GB/s
+    (with FP8 pools the pool bytes count one per element)."""
     import chunked_prefill_paged_gb300 as cpa
     w = W.mixed_step()
     sh = w.shape
@@ -364,6 +385,8 @@ def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush):
     s = w.steps[0]
     params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
                         sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    if fp8:
+        fp8_inputs(cpa, w, t, params, dev)
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
     q, k, v = t.step_inputs(s)
     out = torch.empty_like(q)
@@ -380,11 +403,15 @@ def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
-    byts = w.bytes_per_step()[0]
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError("device error in the mixed step")
+    byts = w.bytes_per_step(1 if fp8 else None)[0]
     gbs = byts / (ms / 1e3) / 1e9
     flops = w.flops_per_step()[0]
     del t
-    return {"workload": w.name, "metric": "mixed-batch algorithmic GB/s", "value": round(gbs, 1), "unit": "GB/s",
+    torch.cuda.empty_cache()
+    return {"workload": w.name + ("_fp8" if fp8 else ""), "metric": "mixed-batch algorithmic GB/s",
+            "value": round(gbs, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "bytes_per_step": byts, "tflops": round(flops / (ms / 1e3) / 1e12, 2),
             "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy"}
 
@@ -398,7 +425,7 @@ def run_case(args, local):
     cpa.load()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    make, idx, rope_theta = CASES[args.case]
+    make, idx, rope_theta, fp8 = CASES[args.case]
     w = make()
     sh = w.shape
     t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
@@ -406,6 +433,8 @@ def run_case(args, local):
     params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
                         sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16 if sh.dtype == "bf16" else cpa.DTYPE_FP32,
                         cpa.FLAG_FUSE_KV_WRITE, rope_theta=rope_theta)
+    if fp8:
+        fp8_inputs(cpa, w, t, params, dev)
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
     q, k, v = t.step_inputs(s)
     out = torch.empty_like(q)
@@ -426,7 +455,7 @@ def run_case(args, local):
         raise RuntimeError("device error")
     ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
     i = idx % len(w.steps)
-    flops, byts = w.flops_per_step()[i], w.bytes_per_step()[i]
+    flops, byts = w.flops_per_step()[i], w.bytes_per_step(1 if fp8 else None)[i]
     return {"case": args.case, "workload": w.name, "steps": args.steps, "warmup": args.warmup, "ms": round(ms, 4),
             "tflops": round(flops / (ms / 1e3) / 1e12, 1), "gbs": round(byts / (ms / 1e3) / 1e9, 1),
             "flops": flops, "bytes": byts, "tokens": int(s.total_new_tokens)}

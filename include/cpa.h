@@ -54,7 +54,8 @@
  *     unspecified result).  The attention then multiplies in fp16: each query
  *     row is scaled by a power of two that puts its largest magnitude in
  *     [2^14, 2^15) (exact for every element within 2^-28 of that maximum)
- *     and the probabilities are rounded to fp16 (finer than bf16).  ("Prefill Processing", Prefix Caching: the KV cache data
+ *     and the probabilities are rounded to fp16 (finer than bf16).
+ *     ("Prefill Optimisation", section 3, prefix caching: the KV cache data
  *     type, e.g. FP8 E4M3, and its quantization scales are part of what the
  *     cached KV means; the pages fix nothing further, so the format and this
  *     encoding are the library's.)

@@ -43,9 +43,10 @@
  * dimension d at position p, each pair (x_c, x_{c+d/2}), c < d/2, turns by
  * the angle p * theta^(-2c/d).
  *
- * FP8 key/value cache (optional, kv_fp8 = 1): "Prefill Processing" names a
- * KV cache data representation (FP8 E4M3) with quantization scales as part
- * of what makes cached KV reusable, and says nothing more.  The reading
+ * FP8 key/value cache (optional, kv_fp8 = 1): "Prefill Optimisation",
+ * section 3 (prefix caching), names a KV cache data representation (FP8
+ * E4M3) with quantization scales as part of what makes cached KV reusable,
+ * and says nothing more.  The reading
  * taken: the pools hold E4M3 codes (the OCP FP8 E4M3 format: 1 sign, 4
  * exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes the
  * subnormals m * 2^-9; S.1111.111 is NaN; no infinities; largest finite

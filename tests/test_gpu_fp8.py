@@ -1,9 +1,10 @@
 """GPU parity for the FP8 (E4M3) key/value cache against the fp64 oracle.
 
-The cache reading ("Prefill Processing", Prefix Caching: the KV data type and
-its quantization scales): a pool element is the E4M3 code of fl32(x / scale)
-for its kv head, a code stands for value * scale, and attention sees every
-key and value -- the chunk's own rows too -- through that encoding.  Checked:
+The cache reading ("Prefill Optimisation", section 3, prefix caching: the KV
+data type and its quantization scales): a pool element is the E4M3 code of
+fl32(x / scale) for its kv head, a code stands for value * scale, and
+attention sees every key and value -- the chunk's own rows too -- through
+that encoding.  Checked:
   * the K/V write (standalone and fused) against the oracle's codes,
     bit-exact, other slots untouched;
   * attention outputs and LSE within the BF16 bounds over mixed batches,

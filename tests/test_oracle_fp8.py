@@ -1,10 +1,10 @@
 """Pins for the oracle's FP8 (E4M3) key/value cache.
 
 The pages name FP8 E4M3 and its quantization scales as one of the things that
-fix what cached KV means ("Prefill Processing", Prefix Caching identity
-dimensions) and say nothing more, so the format is the OCP FP8 E4M3 one (bias
-7, subnormals m * 2^-9, S.1111.111 NaN, largest finite 448) and the cache
-reading is: code = nearest E4M3 value of fl32(x / scale[kv head]), ties to an
+fix what cached KV means ("Prefill Optimisation", section 3, prefix caching:
+the identity dimensions of reusable KV) and say nothing more, so the format is
+the OCP FP8 E4M3 one (bias 7, subnormals m * 2^-9, S.1111.111 NaN, largest
+finite 448) and the cache reading is: code = nearest E4M3 value of fl32(x / scale[kv head]), ties to an
 even mantissa, saturated to +-448; a code stands for value * scale; attention
 sees every key and value (the chunk's own included) through that encoding.
 None of these pins compares the oracle with itself:
