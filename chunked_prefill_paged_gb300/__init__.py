@@ -26,6 +26,8 @@ from .binding import (  # noqa: F401
     SUCCESS,
     Batch,
     CpaError,
+    Engine,
+    StepPlan,
     Params,
     attention,
     chunked_prefill_attention,

@@ -77,7 +77,40 @@ class _Params(ctypes.Structure):
     ]
 
 
+class _EngineConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("max_batched_tokens", ctypes.c_int32),
+        ("chunk_size", ctypes.c_int32),
+        ("scope_key", ctypes.c_uint64),
+    ]
+
+
+class _StepPlan(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("total_new_tokens", ctypes.c_int32),
+        ("request_ids", ctypes.POINTER(ctypes.c_int64)),
+        ("cached_seq_len", ctypes.POINTER(ctypes.c_int32)),
+        ("num_new_tokens", ctypes.POINTER(ctypes.c_int32)),
+        ("cu_new_tokens", ctypes.POINTER(ctypes.c_int32)),
+        ("block_table", ctypes.POINTER(ctypes.c_int32)),
+        ("token_ids", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
 EXPORTED = [
+    "cpa_engine_create",
+    "cpa_engine_destroy",
+    "cpa_engine_add_request",
+    "cpa_engine_schedule",
+    "cpa_engine_commit",
+    "cpa_engine_num_free_blocks",
+    "cpa_engine_num_unfinished",
+    "cpa_engine_prefix_hit_tokens",
     "chunked_prefill_workspace_size",
     "paged_kv_write",
     "chunked_prefill_attention",
@@ -115,6 +148,22 @@ def load(path: str = LIB_PATH):
     lib.cpa_status_string.argtypes = [ctypes.c_int]
     lib.cpa_version.restype = ctypes.c_int32
     lib.cpa_version.argtypes = []
+    lib.cpa_engine_create.restype = ctypes.c_int
+    lib.cpa_engine_create.argtypes = [P(_EngineConfig), P(VP)]
+    lib.cpa_engine_destroy.restype = None
+    lib.cpa_engine_destroy.argtypes = [VP]
+    lib.cpa_engine_add_request.restype = ctypes.c_int
+    lib.cpa_engine_add_request.argtypes = [VP, ctypes.c_int64, VP, ctypes.c_int32, ctypes.c_int32]
+    lib.cpa_engine_schedule.restype = ctypes.c_int
+    lib.cpa_engine_schedule.argtypes = [VP, P(_StepPlan)]
+    lib.cpa_engine_commit.restype = ctypes.c_int
+    lib.cpa_engine_commit.argtypes = [VP, VP]
+    lib.cpa_engine_num_free_blocks.restype = ctypes.c_int32
+    lib.cpa_engine_num_free_blocks.argtypes = [VP]
+    lib.cpa_engine_num_unfinished.restype = ctypes.c_int32
+    lib.cpa_engine_num_unfinished.argtypes = [VP]
+    lib.cpa_engine_prefix_hit_tokens.restype = ctypes.c_int32
+    lib.cpa_engine_prefix_hit_tokens.argtypes = [VP, ctypes.c_int64]
     _lib = lib
     return lib
 
@@ -256,3 +305,87 @@ def attention(batch: Batch, params: Params, q, k_new, v_new, k_cache, v_cache, *
     ws = torch.empty((max(n, 16) + 3) // 4, dtype=torch.float32, device=q.device) if n else None
     chunked_prefill_attention(batch, params, q, k_new, v_new, k_cache, v_cache, out, lse, ws, stream)
     return out, lse
+
+
+@dataclasses.dataclass
+class StepPlan:
+    """One step's batch from the engine (host arrays, copied out)."""
+    request_ids: np.ndarray      # int64 [num_reqs]
+    cached_seq_len: np.ndarray   # int32 [num_reqs]
+    num_new_tokens: np.ndarray   # int32 [num_reqs]
+    block_table: np.ndarray      # int32 [num_reqs, max_blocks_per_seq]
+    token_ids: np.ndarray        # int32 [total_new_tokens]
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.request_ids.shape[0])
+
+
+class Engine:
+    """The library's host-side serving harness (include/cpa_engine.h): greedy
+    token budget, incremental block allocation, prefix hash chain."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int, max_batched_tokens: int,
+                 chunk_size: int, scope_key: int = 0):
+        self._lib = load()
+        cfg = _EngineConfig(num_blocks, block_size, max_blocks_per_seq, max_batched_tokens, chunk_size,
+                            scope_key)
+        h = ctypes.c_void_p()
+        rc = self._lib.cpa_engine_create(ctypes.byref(cfg), ctypes.byref(h))
+        if rc != SUCCESS:
+            raise CpaError(rc, "cpa_engine_create")
+        self._h = h
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self._n = 0
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.cpa_engine_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_request(self, request_id: int, prompt: Sequence[int], max_new_tokens: int) -> None:
+        p = np.ascontiguousarray(np.asarray(prompt, dtype=np.int32))
+        rc = self._lib.cpa_engine_add_request(self._h, int(request_id), p.ctypes.data, int(p.shape[0]),
+                                              int(max_new_tokens))
+        if rc != SUCCESS:
+            raise CpaError(rc, "cpa_engine_add_request")
+
+    def schedule(self) -> StepPlan:
+        pl = _StepPlan()
+        rc = self._lib.cpa_engine_schedule(self._h, ctypes.byref(pl))
+        if rc != SUCCESS:
+            raise CpaError(rc, "cpa_engine_schedule")
+        n, cols, t = pl.num_reqs, pl.max_blocks_per_seq, pl.total_new_tokens
+        self._n = n
+
+        def arr(ptr, count, dtype):
+            if count == 0:
+                return np.zeros(0, dtype=dtype)
+            return np.ctypeslib.as_array(ptr, shape=(count,)).astype(dtype, copy=True)
+
+        return StepPlan(arr(pl.request_ids, n, np.int64), arr(pl.cached_seq_len, n, np.int32),
+                        arr(pl.num_new_tokens, n, np.int32), arr(pl.block_table, n * cols, np.int32).reshape(n, cols),
+                        arr(pl.token_ids, t, np.int32))
+
+    def commit(self, sampled_tokens: Sequence[int]) -> None:
+        s = np.ascontiguousarray(np.asarray(sampled_tokens, dtype=np.int32))
+        if s.shape[0] != self._n:
+            raise ValueError("one sampled token per scheduled request")
+        rc = self._lib.cpa_engine_commit(self._h, s.ctypes.data if self._n else None)
+        if rc != SUCCESS:
+            raise CpaError(rc, "cpa_engine_commit")
+
+    def num_free_blocks(self) -> int:
+        return int(self._lib.cpa_engine_num_free_blocks(self._h))
+
+    def num_unfinished(self) -> int:
+        return int(self._lib.cpa_engine_num_unfinished(self._h))
+
+    def prefix_hit_tokens(self, request_id: int) -> int:
+        return int(self._lib.cpa_engine_prefix_hit_tokens(self._h, int(request_id)))

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcpa.so")
-SOURCES = ["cpa_api.cu", "kernels_basic.cu", "attn_tc.cu", "cpa_no_alloc.cu"]
+SOURCES = ["cpa_api.cu", "kernels_basic.cu", "attn_tc.cu", "cpa_no_alloc.cu", "engine.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +34,8 @@ def _flags():
 
 
 def _newest_input() -> float:
-    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "cpa.h")]
+    inc = os.path.join(ROOT, "include")
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(inc, f) for f in os.listdir(inc)]
     return max(os.path.getmtime(p) for p in paths)
 
 
