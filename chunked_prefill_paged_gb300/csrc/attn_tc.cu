@@ -939,8 +939,17 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
 template <int D, bool F8>
 cudaError_t launch_tc(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_t stream) {
     constexpr int smem = TcCfg<D, F8>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // set once per device (a repeated set is harmless), so that later calls
+    // make no attribute call and can be captured into a CUDA graph
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
     attn_tc_kernel<D, F8><<<grid, TcRoles<F8>::kThreads, smem, stream>>>(a, m.q, m.k_new, m.v_new, m.k_pool,
                                                                           m.v_pool);
     return cudaGetLastError();
