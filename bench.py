@@ -27,6 +27,8 @@ under ncu and per-configuration timing) and prints {"case": ..., "ms": ...}:
   prefix_cache       16 requests sharing a 4096-token cached prefix
   speculative_decode 64 requests x 5 tokens (1 + 4 drafts) over contexts U{1024..32768}
   *_fp8              mixed_step, llama_chunk, speculative_decode over FP8 (E4M3) pools
+  serving            the library's engine driving many steps: 64 requests on four shared
+                     1024-token system prompts (prefix caching), budget 2048, chunk 512
 """
 from __future__ import annotations
 
@@ -89,7 +91,7 @@ def parse_args():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--case", choices=sorted(CASES), default=None,
+    ap.add_argument("--case", choices=sorted(CASES) + ["serving"], default=None,
                     help="time one attention call of this workload step instead of the bench step")
     return ap.parse_args()
 
@@ -461,6 +463,78 @@ def run_case(args, local):
             "flops": flops, "bytes": byts, "tokens": int(s.total_new_tokens)}
 
 
+def run_serving(args, local):
+    """Whole serving iterations through the library's engine: its plan, the
+    batch's one host-to-device copy, a stand-in model's q / k / v (token and
+    position tables on the device), the attention call (K/V write fused) and
+    the commit.  Reports tokens per second of the whole loop and the share
+    the attention call takes."""
+    import chunked_prefill_paged_gb300 as cpa
+    from chunked_prefill_paged_gb300 import build
+    from chunked_prefill_paged_gb300.serving import Server
+    build.build()
+    cpa.load()
+    dev = torch.device("cuda", local)
+    hq, hkv, d, bs = 32, 8, 128, 16
+    vocab, max_pos = 1000, 4096
+    num_reqs, budget, chunk, max_new = 64, 2048, 512, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(1007)
+    tab = lambda n, h: (torch.randn(n, h, d, generator=g, device=dev) * 0.5).to(torch.bfloat16)
+    tq, pq, tk, pk, tv, pv = tab(vocab, hq), tab(max_pos, hq), tab(vocab, hkv), tab(max_pos, hkv), tab(vocab, hkv), \
+        tab(max_pos, hkv)
+    rng = np.random.default_rng(1007)
+    systems = [rng.integers(0, vocab, size=1024) for _ in range(4)]
+    prompts = [np.concatenate([systems[i % 4], rng.integers(0, vocab, size=int(rng.integers(128, 1025)))])
+               for i in range(num_reqs)]
+    cols = (max(len(p) for p in prompts) + max_new) // bs + 1
+    num_blocks = sum(len(p) + max_new for p in prompts) // bs + num_reqs + 1
+    eng = cpa.Engine(num_blocks, bs, cols, budget, chunk, scope_key=1007)
+    for i, p in enumerate(prompts):
+        eng.add_request(i, p, max_new)
+    params = cpa.Params(hq, hkv, d, bs, num_blocks, 1024, 1.0 / np.sqrt(d), cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    k_cache = torch.zeros((num_blocks, bs, hkv, d), dtype=torch.bfloat16, device=dev)
+    v_cache = torch.zeros_like(k_cache)
+    server = Server(eng, params, k_cache, v_cache, max_reqs=num_reqs, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    attn_ev = []
+
+    def make_qkv(plan):
+        pos = np.concatenate([np.arange(c, c + n) for c, n in zip(plan.cached_seq_len, plan.num_new_tokens)])
+        ti = torch.from_numpy(plan.token_ids.astype(np.int64)).pin_memory().to(dev, non_blocking=True)
+        pi = torch.from_numpy(pos.astype(np.int64)).pin_memory().to(dev, non_blocking=True)
+        q, k, v = tq[ti] + pq[pi], tk[ti] + pk[pi], tv[ti] + pv[pi]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn_ev.append(e0)
+        return q, k, v
+
+    def sample(plan, out):
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        attn_ev.append(e1)
+        return rng.integers(0, vocab, size=plan.num_reqs)
+
+    steps = tokens = 0
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    while eng.num_unfinished() > 0 and steps < 5000:
+        plan, out, _ = server.step(make_qkv, sample)
+        steps += 1
+        tokens += int(plan.num_new_tokens.sum())
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError("device error")
+    attn_ms = sum(attn_ev[i].elapsed_time(attn_ev[i + 1]) for i in range(0, len(attn_ev) - 1, 2))
+    return {"case": "serving", "requests": num_reqs, "steps": steps, "tokens": tokens,
+            "tokens_per_s": round(tokens / wall, 1), "ms_per_step": round(wall * 1e3 / max(steps, 1), 4),
+            "attention_ms_per_step": round(attn_ms / max(steps, 1), 4),
+            "attention_share": round(attn_ms / (wall * 1e3), 3),
+            "config": {"H_q": hq, "H_kv": hkv, "head_dim": d, "block_size": bs, "budget": budget, "chunk": chunk,
+                       "system_prompts": "4 x 1024 tokens", "suffix": "U{128..1024}", "max_new_tokens": max_new}}
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands on the host cores, same metric and workload;
     each step a bounded sample."""
@@ -498,7 +572,8 @@ def main():
     args = parse_args()
     rank, world, local = dist_setup()
     if args.case is not None:
-        line = run_case(args, local) if rank == 0 else None
+        runner = run_serving if args.case == "serving" else run_case
+        line = runner(args, local) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
