@@ -110,6 +110,7 @@ struct __align__(8) TcShared {
     // counter and passes them to the other roles through this ring
     uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
     int unit_ring[kUnitRing];
+    Unit unit_desc[kUnitRing];  // the decoded unit of each ring slot
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -262,15 +263,34 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// A decoded unit through a ring slot: the scheduling warp decodes each unit
+// once, as soon as it has claimed it, and every other role copies the fields
+// (the slot's mbarrier orders the stores before the loads).
+__device__ __forceinline__ void put_unit(Unit &dst, const Unit &u) {
+    volatile int *d = reinterpret_cast<volatile int *>(&dst);
+    const int *v = reinterpret_cast<const int *>(&u);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(Unit) / 4); ++k) d[k] = v[k];
+}
+__device__ __forceinline__ void get_unit(Unit &u, const Unit &src) {
+    const volatile int *d = reinterpret_cast<const volatile int *>(&src);
+    int *v = reinterpret_cast<int *>(&u);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(Unit) / 4); ++k) v[k] = d[k];
+}
+
 // The i-th unit of this CTA, as published by the scheduling warp (every lane
-// of the calling warp takes part).  Returns a value >= the unit count when
-// the CTA is done, and -1 when the wait gave up (timeout or abort).
-__device__ __forceinline__ int read_unit(TcShared &sh, int i, long long limit, const volatile int *abort_flag) {
+// of the calling warp takes part): its index, and for an attention unit its
+// decoded fields in u.  The index is >= the unit count for a piece of the K/V
+// write or when the CTA is done; -1 when the wait gave up (timeout or abort).
+__device__ __forceinline__ int read_unit(TcShared &sh, int i, long long limit, const volatile int *abort_flag,
+                                         Unit &u) {
     const int s = i % kUnitRing;
     if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.unit_full[s], (uint32_t)((i / kUnitRing) & 1), limit,
                                                     abort_flag)))
         return -1;
     const int unit = *reinterpret_cast<volatile int *>(&sh.unit_ring[s]);
+    get_unit(u, sh.unit_desc[s]);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.unit_empty[s]);
     return unit;
@@ -373,6 +393,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         int taken = (kv_role == 0 && lane == 0) ? atomicAdd(a.sched, 1) : 0;
         for (int it = 0;; ++it) {  // it: units started by this CTA
             int unit;
+            Unit u;
             if (kv_role == 0) {
                 unit = __shfl_sync(0xffffffffu, taken, 0);
                 const int s = it % kUnitRing;
@@ -382,14 +403,16 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (unit < total_units) decode_unit(a, unit, u);  // once, for every role
                 if (lane == 0) {
+                    put_unit(sh.unit_desc[s], u);
                     sh.unit_ring[s] = unit;
-                    mbar_arrive(&sh.unit_full[s]);  // release: the index is visible to every waiter
+                    mbar_arrive(&sh.unit_full[s]);  // release: index and fields are visible to every waiter
                     // pieces of the K/V write need no copies: claim the next index now
                     if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
                 }
             } else {
-                unit = read_unit(sh, it, LIM, abort_flag);
+                unit = read_unit(sh, it, LIM, abort_flag, u);
                 if (unit < 0) {
                     ok = false;
                     break;
@@ -398,8 +421,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             if (unit >= end_index) break;
             if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
-            Unit u;
-            decode_unit(a, unit, u);
             TileList tl;
             tl.init(u);
             const int n = tl.n_total;
@@ -539,7 +560,8 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         const uint32_t tO = tmem + kTmemO;
         const bool s_role = (warp == kMmaWarp);
         for (int ucnt = 0;; ++ucnt) {  // ucnt: units started
-            const int unit = read_unit(sh, ucnt, LIM, abort_flag);
+            Unit u;
+            const int unit = read_unit(sh, ucnt, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -547,8 +569,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             if (unit >= end_index) break;
             if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
-            Unit u;
-            decode_unit(a, unit, u);
             TileList tl;
             tl.init(u);
             const int n = tl.n_total;
@@ -671,7 +691,8 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         uint32_t phb = 0;
         bool ok = true;
         for (int cc = 0;; ++cc) {
-            const int unit = read_unit(sh, cc, LIM, abort_flag);
+            Unit u;
+            const int unit = read_unit(sh, cc, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -679,8 +700,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             if (unit >= end_index) break;
             if (unit >= total_units) continue;
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
-            Unit u;
-            decode_unit(a, unit, u);
             TileList tl;
             tl.init(u);
             for (int j = 0; j < tl.n_total; ++j) {
@@ -722,7 +741,8 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         uint32_t prev_ph = 0;
         bool ok = true;
         for (int oc = 0;; ++oc) {  // oc: units started
-            const int unit = read_unit(sh, oc, LIM, abort_flag);
+            Unit u;
+            const int unit = read_unit(sh, oc, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -740,8 +760,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 continue;
             }
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
-            Unit u;
-            decode_unit(a, unit, u);
             TileList tl;
             tl.init(u);
             const int n = tl.n_total;
