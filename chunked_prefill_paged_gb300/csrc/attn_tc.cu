@@ -1,6 +1,7 @@
 // attn_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) attention over the paged
-// K/V cache for BF16.  Persistent: one CTA per SM takes work units (see
-// cpa_internal.h) from a per-launch counter in the workspace, in index
+// K/V cache: BF16 pools (attn_tc_kernel<D, false>) and FP8 E4M3 pools
+// (attn_tc_kernel<128, true>).  Persistent: one CTA per SM takes work units
+// (see cpa_internal.h) from a per-launch counter in the workspace, in index
 // order (a request's heaviest units first), so that CTAs that finish early
 // take more units.
 //
@@ -14,7 +15,7 @@
 // across 128-key tiles; a split unit (one piece of a decode's keys) writes
 // its unnormalised partial for attn_merge instead.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; 512 with FP8 pools):
 //   warps 0-7  softmax / correction / epilogue.  Two threads own one query
 //              row: warp w covers TMEM lanes 32 (w % 4) + 16 (w / 4) .. +15,
 //              its threads 0-15 the row's keys 0-63 (output columns 0 .. D/2-1)
@@ -24,7 +25,9 @@
 //              the work counter, so CTAs whose attention work has run out take
 //              them (this kernel reads new keys from k_new / v_new, so the
 //              pool rows are only needed by the next call).
-//   warp 8     TMA producer of Q per unit and of the K tiles; warp 10 of the V
+//   warp 8     unit scheduler (it claims each unit, decodes it once and passes
+//              the decoded unit to the other roles through a ring) and TMA
+//              producer of Q per unit and of the K tiles; warp 10 of the V
 //              tiles, each into its own ring, so a V slot still in use never
 //              holds up the next K copy.  A pool tile is one box per cache
 //              block (found through the block table), a new-token tile one
@@ -35,9 +38,11 @@
 //   warp 11    PV MMA issuer: O += P(j) V(j) once the softmax has written P(j).
 //              Issuing from two warps on different SM sub-partitions halves
 //              the instruction stream each shares with the softmax warps.
+//   warps 12-15 (FP8 pools only) expand E4M3 code tiles in place into the
+//              fp16 tiles the MMAs read (K: 12-13, V: 14-15).
 //
 // TMEM (512 columns): three score buffers S0 [0,128), S1 [128,256) and
-// S2 [256,384), O [384, 384 + D).  P(j), as bf16 pairs, overwrites the first
+// S2 [256,384), O [384, 384 + D).  P(j), as bf16 (fp16) pairs, overwrites the first
 // 64 columns of the buffer that held S(j); S(j+3) reuses that buffer only
 // after PV(j) has completed.  With three buffers the chain softmax(j) ->
 // PV(j) -> S(j+3) -> softmax(j+3) spans two other softmax tiles.  Rescaling is lazy:
@@ -120,38 +125,6 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
-// 2^x for a pair of arguments on the FMA pipe instead of the MUFU unit,
-// by Cody-Waite range reduction and a polynomial: x = n + f with n the
-// nearest integer (the 1.5 * 2^23 rounding constant) and f in [-1/2, 1/2];
-// 2^f comes from a degree-3 polynomial fitted here for minimax relative
-// error (Lawson's iteratively reweighted least squares; max relative error
-// 7.5e-5, well under bf16's 2^-9), and 2^n is added to the exponent field.
-// Arguments below -126 are clamped there, which yields a value of at most
-// 2^-125 in place of the exact (smaller) one.
-constexpr float kExp2C0 = 0.99992809f;
-constexpr float kExp2C1 = 0.69326099f;
-constexpr float kExp2C2 = 0.24261081f;
-constexpr float kExp2C3 = 0.05517144f;
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -126.0f);
-    x.y = fmaxf(x.y, -126.0f);
-    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));       // n in the low mantissa bits
-    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));     // n as a float
-    const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);      // x - n
-    float2 p = __ffma2_rn(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-    p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
-    p = __ffma2_rn(p, f, make_float2(kExp2C0, kExp2C0));
-    // (bits of t) << 23 == n << 23 modulo 2^32: the constant's own bits shift out
-    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
-}
-
-#ifndef CPA_POLY_PAIRS
-#define CPA_POLY_PAIRS 0  // of the 32 exponential pairs per thread and tile
-#endif
-__host__ __device__ constexpr bool poly_pair(int i) { return (i * CPA_POLY_PAIRS) % 32 < CPA_POLY_PAIRS; }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -843,21 +816,15 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
                 {
-                    // exponentials in pairs: most on the MUFU unit, the pairs
-                    // poly_pair() picks on the FMA pipe, so that neither unit
-                    // alone sets the pace
+                    // exponentials in pairs: paired FMAs and adds, ex2 on the MUFU
                     uint32_t r[32];
                     const float2 sl2 = make_float2(sl, sl), neg2 = make_float2(neg, neg);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sl2, neg2);
                         float2 e;
-                        if (poly_pair(i)) {
-                            e = exp2_poly2(x);
-                        } else {
-                            e.x = ex2(x.x);
-                            e.y = ex2(x.y);
-                        }
+                        e.x = ex2(x.x);
+                        e.y = ex2(x.y);
                         if (i & 1)
                             acc1 = __fadd2_rn(acc1, e);
                         else

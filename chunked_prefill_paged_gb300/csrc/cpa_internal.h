@@ -116,8 +116,9 @@ struct AttnArgs {
     int write_chunks;   // tensor-core kernel with the fused write: indices [units, units +
                         // write_chunks) of the counter are pieces of the K/V write, taken
                         // by CTAs whose attention work has run out
-    int fuse_write;     // write new K/V into the pool in the prologue
-    int write_ctas;     // CTAs that share the fused write
+    int fuse_write;     // write new K/V into the pool in the same launch
+    int write_ctas;     // grid size: the tensor-core kernel's persistent CTAs (units and
+                        // write pieces, at most one per SM); the CUDA-core kernel's units
     int *err;           // device error word (first error wins)
     long long timeout_cycles;
     int test_stall;     // testing only: withhold the first K tile's copies
