@@ -397,6 +397,12 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             TileList tl;
             tl.init(u);
             const int n = tl.n_total;
+            // in a batch that mixes prefill and decode units, a decode piece's
+            // cached K/V (read once) may leave L2 first, ahead of the prefill
+            // units' K/V that other query tiles read again; elsewhere the
+            // copies take no policy
+            const bool hinted = a.interleave && u.piece >= 0;
+            const uint64_t pol = hinted ? policy_evict_first() : 0;
             // The warp runs converged: every lane takes the waits, lane 0 arms
             // the barriers, and the copies of one tile are spread over the lanes
             // (one cache block and 64-column half per lane).
@@ -426,7 +432,11 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                             record_error(a.err, kErrBadBlock);
                             blk = 0;  // keep the byte count; this unit's output is void
                         }
-                        tma_load_4d(dst + b * a.bs * D, kv ? &tm_v_pool : &tm_k_pool, full, 0, u.g, 0, blk);
+                        if (hinted)
+                            tma_load_4d_hint(dst + b * a.bs * D, kv ? &tm_v_pool : &tm_k_pool, full, 0, u.g, 0, blk,
+                                             pol);
+                        else
+                            tma_load_4d(dst + b * a.bs * D, kv ? &tm_v_pool : &tm_k_pool, full, 0, u.g, 0, blk);
                     }
                 } else if (F8) {
                     // the new rows' codes: one 128-row box of the workspace copy
@@ -446,8 +456,12 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                             record_error(a.err, kErrBadBlock);
                             blk = 0;  // keep the byte count; this unit's output is void
                         }
-                        tma_load_4d(dst + h * HB + b * a.bs * 128, kv ? &tm_v_pool : &tm_k_pool, full, h * 64, u.g,
-                                    0, blk);
+                        if (hinted)
+                            tma_load_4d_hint(dst + h * HB + b * a.bs * 128, kv ? &tm_v_pool : &tm_k_pool, full,
+                                             h * 64, u.g, 0, blk, pol);
+                        else
+                            tma_load_4d(dst + h * HB + b * a.bs * 128, kv ? &tm_v_pool : &tm_k_pool, full, h * 64,
+                                        u.g, 0, blk);
                     }
                 } else {
                     if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)TB);

@@ -431,6 +431,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.tile_m = pl.tile_m;
     a.tiles_per_unit = pl.tiles_per_unit;
     a.head_major = pl.head_major;
+    a.interleave = (pl.tile_m == kTcTileM && pl.direct_units > 0 && pl.split_units > 0) ? 1 : 0;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
     a.q = q;

@@ -103,6 +103,9 @@ struct AttnArgs {
                         // (else kv head innermost); see decode_unit
     int num_direct_units;
     int num_split_units;
+    int interleave;     // tensor-core kernel, batches with both kinds: direct and split units
+                        // alternate over the index range (see decode_unit), so that prefill
+                        // (tensor-bound) and decode (HBM-bound) units run side by side
     // data
     const void *q;
     const void *k_new;

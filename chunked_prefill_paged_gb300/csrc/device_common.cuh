@@ -42,8 +42,17 @@ struct Unit {
 // gets the same result.  Returns false for an index past the last unit.
 __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u) {
     const int lane = threadIdx.x & 31;
-    const bool split = unit >= a.num_direct_units;
-    const int target = split ? unit - a.num_direct_units : unit;
+    bool split = unit >= a.num_direct_units;
+    int target = split ? unit - a.num_direct_units : unit;
+    if (a.interleave && unit < a.num_direct_units + a.num_split_units) {
+        // direct (prefill) and split (decode) units spread evenly over the
+        // index range, each kind in its own order: index k is direct when
+        // floor((k + 1) D / T) > floor(k D / T), D direct units of T in all
+        const long long D = a.num_direct_units, T = a.num_direct_units + (long long)a.num_split_units;
+        const long long before = (long long)unit * D / T, after = ((long long)unit + 1) * D / T;
+        split = after == before;
+        target = split ? (int)(unit - before) : (int)before;
+    }
     int base = 0;
     long long base_ws = 0;
     for (int r0 = 0; r0 < a.num_reqs; r0 += 32) {
