@@ -227,6 +227,27 @@ class Batch:
         self.cu = torch.from_numpy(cu).to(dev)
         self.block_table = torch.from_numpy(bt).to(dev)
 
+    @classmethod
+    def from_device(cls, h_cached_seq_len: np.ndarray, h_num_new_tokens: np.ndarray, h_block_table: np.ndarray,
+                    cached_seq_len: torch.Tensor, num_new_tokens: torch.Tensor, cu_new_tokens: torch.Tensor,
+                    block_table: torch.Tensor) -> "Batch":
+        """A batch whose device arrays already exist (int32, contiguous; e.g.
+        filled by one host-to-device copy), with host mirrors of the same
+        values."""
+        b = cls.__new__(cls)
+        b.h_cached = np.ascontiguousarray(h_cached_seq_len, dtype=np.int32)
+        b.h_new = np.ascontiguousarray(h_num_new_tokens, dtype=np.int32)
+        b.h_block_table = np.ascontiguousarray(h_block_table, dtype=np.int32)
+        cu = np.zeros(len(b.h_new) + 1, dtype=np.int32)
+        np.cumsum(b.h_new, out=cu[1:])
+        b.h_cu = cu
+        n, cols = b.h_block_table.shape
+        for t, size in ((cached_seq_len, n), (num_new_tokens, n), (cu_new_tokens, n + 1), (block_table, n * cols)):
+            if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() != size:
+                raise ValueError("device arrays must be contiguous int32 of the batch's sizes")
+        b.cached, b.new, b.cu, b.block_table = cached_seq_len, num_new_tokens, cu_new_tokens, block_table
+        return b
+
     @property
     def num_reqs(self) -> int:
         return int(self.h_cached.shape[0])

@@ -51,16 +51,8 @@ class StepBuffers:
             ev.record(stream)
         self.done[i] = ev
         d = self.dev[i]
-        b = Batch.__new__(Batch)
-        b.h_cached = plan.cached_seq_len.copy()
-        b.h_new = plan.num_new_tokens.copy()
-        b.h_cu = cu
-        b.h_block_table = plan.block_table
-        b.cached = d[0:nr]
-        b.new = d[nr:2 * nr]
-        b.cu = d[2 * nr:3 * nr + 1]
-        b.block_table = d[3 * nr + 1:3 * nr + 1 + nr * self.cols]
-        return b
+        return Batch.from_device(plan.cached_seq_len, plan.num_new_tokens, plan.block_table, d[0:nr], d[nr:2 * nr],
+                                 d[2 * nr:3 * nr + 1], d[3 * nr + 1:3 * nr + 1 + nr * self.cols])
 
 
 class Server:
