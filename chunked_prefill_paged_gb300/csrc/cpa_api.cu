@@ -381,13 +381,16 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
     const float *q_rscale = nullptr;
-    if (params->rope_theta > 0.f || kv_fp8(params)) {
+    const bool prepass = params->rope_theta > 0.f || kv_fp8(params);
+    RopeArgs r{};
+    if (prepass) {
         // pre-pass over the new rows: rotate q and k_new, encode the keys and
         // values for the FP8 cache, into workspace copies that the attention
         // then reads (and, for a fused write, put the rows as the pool holds
-        // them into their slots)
+        // them into their slots).  Launched below, once every host-side step
+        // that can fail is done.
         char *ws = static_cast<char *>(workspace);
-        RopeArgs r = rope_args(batch, params, dev.err);
+        r = rope_args(batch, params, dev.err);
         r.q = q;
         r.k_new = k_new;
         r.v_new = v_new;
@@ -400,7 +403,6 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         r.write_pool = fuse_write ? 1 : 0;
         r.k_cache = k_cache;
         r.v_cache = v_cache;
-        if (launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
         if (r.q_rot) q = r.q_rot;
         if (r.k_rot) k_new = r.k_rot;
         if (r.kv_fp8) {
@@ -465,11 +467,15 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     if (pl.tile_m == kTcTileM) {
         TcMaps maps;
         if (cpa_status s = make_tc_maps(batch, params, q, k_new, v_new, k_cache, v_cache, maps)) return s;
+        if (prepass && launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
         a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
         e = cudaMemsetAsync(a.sched, 0, sizeof(int), st);
         if (e == cudaSuccess) e = launch_attn_tc(a, maps, st);
     } else {
-        e = launch_attn_simt(a, params->dtype, st);
+        // the CUDA-core kernel (its pre-pass is RoPE only: FP8 pools need the
+        // tensor-core kernel)
+        e = prepass ? launch_rope(r, dev.sms, st) : cudaSuccess;
+        if (e == cudaSuccess) e = launch_attn_simt(a, params->dtype, st);
     }
     if (e != cudaSuccess) return CPA_ERR_CUDA;
     if (pl.split_reqs > 0) {

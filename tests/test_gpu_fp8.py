@@ -260,3 +260,22 @@ def test_every_code_scores_exactly_through_the_key_path(cpa):
             got = lse[tok].numpy().astype(np.float64)
             err = np.abs(got - want)
             assert np.all(err <= 2e-6 * np.maximum(1.0, np.abs(want))), (name, codes, got, want)
+
+
+@pytest.mark.parametrize("bs,hq", [(32, 16), (64, 64)])
+def test_fp8_other_block_sizes_and_groups(cpa, bs, hq):
+    # block sizes 32 / 64 (several code boxes per key tile) and G = 8 query
+    # heads per kv head (the long-context shape)
+    w = W.make_batch_workload(f"fp8_b{bs}", W.Shape(hq, 8 if hq == 64 else 4, 128, bs, 1024, "bf16"),
+                              [(0, 150), (2000, 1), (513, 64), (4096, 1)], seed=67)
+    res = run_fp8(cpa, w)
+    assert_within(res, "bf16")
+
+
+def test_fp8_speculative_decode_queries(cpa):
+    # multi-token decode queries (1 + draft tokens) over long FP8 contexts:
+    # short causal chunks on the split path
+    w = W.make_batch_workload("fp8_spec", W.Shape(32, 8, 128, 16, 1024, "bf16"),
+                              [(3000, 5), (9000, 5), (17, 5), (12345, 3)], seed=68)
+    res = run_fp8(cpa, w)
+    assert_within(res, "bf16")
