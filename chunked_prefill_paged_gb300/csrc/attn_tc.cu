@@ -236,6 +236,77 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// The 16 output rows [lr0, lr0 + 16) of a unit run as tail pieces, merged by
+// one warp from the pieces' partials: each holds O_q = sum over its keys of
+// 2^(s - m_q) v (times the value scale), m_q and l_q; a row is
+// sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q with M the largest m_q of the
+// pieces that saw a key.  Lane j < 16 forms row lr0 + j's weights; the rows
+// are then read whole (D floats over the warp's lanes, from L2, where the
+// other CTAs' partials are) and written as bf16.
+template <int D>
+__device__ __forceinline__ void merge_tail_rows(const AttnArgs &a, const Unit &u, int lr0, int lane) {
+    constexpr int F = D / 4;     // float4 per row
+    constexpr int RPP = 32 / F;  // rows per pass
+    const int P = a.tail_pieces;
+    const long long pf = partial_floats(a.tile_m, D);
+    const float *base = a.ws + a.tail_ws + (long long)u.tail * P * pf;
+    const long long ml = (long long)u.rows * D;  // row maxima, then sums
+    float w[kMaxTailPieces];
+    float inv;
+    {
+        const int r = lr0 + (lane & 15);
+        const bool valid = r < u.rows;
+        float mq[kMaxTailPieces], lq[kMaxTailPieces], M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kMaxTailPieces; ++q) {
+            lq[q] = (q < P && valid) ? __ldcg(base + q * pf + ml + u.rows + r) : 0.f;
+            mq[q] = lq[q] > 0.f ? __ldcg(base + q * pf + ml + r) : -INFINITY;
+            M = fmaxf(M, mq[q]);
+        }
+        float L = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxTailPieces; ++q) {
+            w[q] = lq[q] > 0.f ? ex2(mq[q] - M) : 0.f;
+            L = fmaf(lq[q], w[q], L);
+        }
+        inv = L > 0.f ? 1.f / L : 0.f;
+        if (lane < 16 && valid && a.lse) {
+            const int pr = u.row0 + r;
+            a.lse[(long long)(u.cu0 + pr / a.G) * a.hq + u.g * a.G + pr % a.G] =
+                (M + __log2f(L)) * 0.69314718055994531f;
+        }
+    }
+    const int sub = lane / F, f = lane % F;
+#pragma unroll 4
+    for (int i = 0; i < 16; i += RPP) {
+        const int j = i + sub;
+        float wj[kMaxTailPieces];
+#pragma unroll
+        for (int q = 0; q < kMaxTailPieces; ++q) wj[q] = __shfl_sync(0xffffffffu, w[q], j);
+        const float invj = __shfl_sync(0xffffffffu, inv, j);
+        const int r = lr0 + j;
+        if (r < u.rows) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxTailPieces; ++q) {
+                if (q < P) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + q * pf + (long long)r * D) + f);
+                    acc.x = fmaf(wj[q], v.x, acc.x);
+                    acc.y = fmaf(wj[q], v.y, acc.y);
+                    acc.z = fmaf(wj[q], v.z, acc.z);
+                    acc.w = fmaf(wj[q], v.w, acc.w);
+                }
+            }
+            const int pr = u.row0 + r;
+            const long long t = u.cu0 + pr / a.G, h = u.g * a.G + pr % a.G;
+            uint2 o;
+            o.x = pack_bf16(acc.x * invj, acc.y * invj);
+            o.y = pack_bf16(acc.z * invj, acc.w * invj);
+            reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) + (t * a.hq + h) * D)[f] = o;
+        }
+    }
+}
+
 // A decoded unit through a ring slot: the scheduling warp decodes each unit
 // once, as soon as it has claimed it, and every other role copies the fields
 // (the slot's mbarrier orders the stores before the loads).
@@ -292,7 +363,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const long long LIM = a.timeout_cycles;
-    const int total_units = a.num_direct_units + a.num_split_units;
+    const int total_units = attention_units(a);
     const int end_index = total_units + a.write_chunks;  // then the fused K/V write
 
     if (tid == 0) {
@@ -888,7 +959,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 const int col0 = half * (D / 2) + c * 32;
                 if (row_valid) {
                     if (u.piece >= 0) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.ws + u.ws_off + (long long)pr * D + col0);
+                        float4 *dst = reinterpret_cast<float4 *>(a.ws + u.ws_off + (long long)lr * D + col0);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(__uint_as_float(r[4 * i]) * v_mul, __uint_as_float(r[4 * i + 1]) * v_mul,
@@ -914,10 +985,26 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             if (row_valid && half == 0) {
                 if (u.piece >= 0) {
                     float *ws = a.ws + u.ws_off;
-                    ws[(long long)u.rows * D + pr] = m_ref;
-                    ws[(long long)u.rows * D + u.rows + pr] = l;
+                    ws[(long long)u.rows * D + lr] = m_ref;
+                    ws[(long long)u.rows * D + u.rows + lr] = l;
                 } else if (a.lse) {
                     a.lse[(long long)t * a.hq + h] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+                }
+            }
+            if (u.tail >= 0 && warp_rows) {
+                // a tail piece: the warp that completes the unit's last piece
+                // for its 16 rows (the same warp of every piece's CTA writes
+                // them) merges the pieces' partials of those rows.  The warp
+                // barrier orders the lanes' partial writes before lane 0's
+                // release, and lane 0's acquire before the lanes' reads.
+                __syncwarp();
+                int last = 0;
+                if (lane == 0)
+                    last = atom_add_acq_rel_gpu(a.tail_count + u.tail * kSoftmaxWarpsMax + warp, 1) ==
+                           a.tail_pieces - 1;
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __syncwarp();
+                    merge_tail_rows<D>(a, u, 32 * (warp & 3) + 16 * (warp >> 2), lane);
                 }
             }
         }
@@ -958,7 +1045,7 @@ cudaError_t launch_tc(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_t
 
 cudaError_t launch_attn_tc(const AttnArgs &a, const TcMaps &m, cudaStream_t stream) {
     const int grid = a.write_ctas;  // persistent: min(units + write pieces, SMs)
-    if (grid <= 0 || a.num_direct_units + a.num_split_units == 0) return cudaSuccess;
+    if (grid <= 0 || attention_units(a) == 0) return cudaSuccess;
     if (a.kv_fp8) return a.d == 128 ? launch_tc<128, true>(a, m, grid, stream) : cudaErrorInvalidValue;
     return a.d == 128 ? launch_tc<128, false>(a, m, grid, stream) : launch_tc<64, false>(a, m, grid, stream);
 }

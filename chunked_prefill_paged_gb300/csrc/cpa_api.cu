@@ -5,9 +5,14 @@
 #include <cuda_runtime.h>
 
 #include <math.h>
-#include <mutex>
 #include <stdint.h>
 #include <string.h>
+
+#include <algorithm>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <vector>
 
 #include "../../include/cpa.h"
 #include "cpa_internal.h"
@@ -128,6 +133,9 @@ struct Plan {
     size_t q16_off = 0, qs_off = 0; // FP8 cache: fp16 queries and their row scales
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
+    int tail_units = 0;     // the last direct units run as tail_pieces pieces each
+    int tail_pieces = 0;
+    long long tail_ws_floats = 0;  // float offset of their partials
     int direct_units = 0;
     int split_units = 0;
     int split_reqs = 0;
@@ -143,7 +151,103 @@ cpa_status check_attention_support(const cpa_params *p) {
     return CPA_SUCCESS;
 }
 
-Plan make_plan(const cpa_batch *b, const cpa_params *p) {
+// Cost of a unit in periods of one key tile: its tiles plus the switch to it
+// (the previous unit's last PV and epilogue, refilling the copy pipeline),
+// about six tile periods by clock64 traces of the kernel.  A tail piece costs
+// about twelve periods more (measured: chunks of 2048 query tokens cut this
+// way ran 5 % slower over 2048 cached tokens, as fast over 4096, 3.5 %
+// faster over 6144): its partial's write, the count, and the merge.
+constexpr double kUnitSwitchTiles = 6.0;
+constexpr double kTailPieceTiles = 12.0;
+
+// Greedy list schedule, as the kernel's work counter hands out indices: each
+// of the CTAs (a min-heap of their finish times) takes the next unit when it
+// is free.
+using FinishHeap = std::priority_queue<double, std::vector<double>, std::greater<double>>;
+
+double schedule_end(FinishHeap h) {
+    double end = 0;
+    while (!h.empty()) {
+        end = h.top();
+        h.pop();
+    }
+    return end;
+}
+
+// Tail pieces for a batch of direct units only.  With U units of similar size
+// on S SMs the last wave holds U mod S units and leaves the other SMs idle;
+// cutting those units into p pieces by key tiles (each piece writes a partial,
+// merged by the CTA that finishes the unit's last piece) spreads that work
+// over more SMs.  Simulates the schedule without pieces and with the last k
+// units in p pieces (k the last wave's units, and that plus half the SMs;
+// p = 2, 3, 4) and keeps the best cut if it ends at least 2% sooner.
+void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
+    const int D = pl.direct_units;
+    if (sms <= 0 || D < sms || D > 8 * sms || pl.split_units > 0 ||
+        (p->flags & (CPA_FLAG_NO_SPLIT | CPA_FLAG_NO_TAIL_SPLIT)))
+        return;
+    const int G = p->num_heads_q / p->num_heads_kv, hkv = p->num_heads_kv;
+    // key tiles of every direct unit in index order (the order decode_unit uses)
+    std::vector<int> tiles;
+    tiles.reserve(D);
+    for (int r = 0; r < b->num_reqs; ++r) {
+        const int C = b->h_cached_seq_len[r], N = b->h_num_new_tokens[r];
+        const ReqWork w = request_work(C, N, G, hkv, p->head_dim, pl.tile_m, pl.split_len, pl.tiles_per_unit);
+        const int rows = N * G, n_qt = cdiv(rows, pl.tile_m);
+        for (int local = 0; local < w.direct_units; ++local) {
+            const int i = pl.head_major ? local % n_qt : local / hkv;
+            const int last = n_qt - 1 - i;
+            const int last_tok = (std::min((last + 1) * pl.tile_m, rows) - 1) / G;
+            tiles.push_back(cdiv(C, kTcTileN) + cdiv(last_tok + 1, kTcTileN));
+        }
+    }
+    if ((int)tiles.size() != D) return;
+    const int R = D % sms;
+    std::vector<int> cuts;
+    if (R > 0) cuts.push_back(R);
+    if (R + sms / 2 <= D) cuts.push_back(R + sms / 2);
+    if (cuts.empty()) return;
+    std::sort(cuts.begin(), cuts.end(), std::greater<int>());  // head lengths D - k ascending
+    FinishHeap h;
+    for (int c = 0; c < sms; ++c) h.push(0.0);
+    double best = -1;
+    size_t next_cut = 0;
+    for (int u = 0; u <= D; ++u) {
+        while (next_cut < cuts.size() && D - cuts[next_cut] == u) {
+            const int k = cuts[next_cut++];
+            for (int pieces = 2; pieces <= kMaxTailPieces; ++pieces) {
+                bool fits = true;
+                for (int v = D - k; v < D && fits; ++v) fits = tiles[v] >= 2 * pieces;
+                if (!fits) break;
+                FinishHeap t = h;
+                for (int v = D - k; v < D; ++v) {
+                    for (int q = 0; q < pieces; ++q) {
+                        const int n = (q + 1) * tiles[v] / pieces - q * tiles[v] / pieces;
+                        const double f = t.top() + n + kUnitSwitchTiles + kTailPieceTiles;
+                        t.pop();
+                        t.push(f);
+                    }
+                }
+                const double end = schedule_end(t);
+                if (best < 0 || end < best) {
+                    best = end;
+                    pl.tail_units = k;
+                    pl.tail_pieces = pieces;
+                }
+            }
+        }
+        if (u == D) break;
+        const double f = h.top() + tiles[u] + kUnitSwitchTiles;
+        h.pop();
+        h.push(f);
+    }
+    if (best < 0 || best > 0.98 * schedule_end(h)) {
+        pl.tail_units = 0;
+        pl.tail_pieces = 0;
+    }
+}
+
+Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     Plan pl;
     const bool tc = use_tensor_cores(p);
     pl.tile_m = tc ? kTcTileM : kSimtTileM;
@@ -176,6 +280,11 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
     // K/V of the batch larger than about half of L2: walk the direct units
     // head by head so that concurrent CTAs share K/V tiles in L2
     pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
+    if (tc) plan_tail(b, p, sms, pl);
+    if (pl.tail_units > 0) {
+        pl.tail_ws_floats = pl.ws_floats;
+        pl.ws_floats += (long long)pl.tail_units * pl.tail_pieces * partial_floats(pl.tile_m, p->head_dim);
+    }
     pl.ws_bytes = (size_t)pl.ws_floats * sizeof(float);
     const size_t T = (size_t)b->total_new_tokens, es = (size_t)elem_bytes(p), d = (size_t)p->head_dim;
     auto take = [&](size_t bytes) {  // next 256-byte aligned part of the workspace
@@ -196,9 +305,11 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p) {
         pl.rk_off = take(T * p->num_heads_kv * d * es);
     }
     if (tc) {
-        // the persistent kernel's work counter, after the partials
+        // the persistent kernel's work counter and the tail units' counters,
+        // after the partials
         pl.sched_off = (pl.ws_bytes + 255) & ~(size_t)255;
-        pl.ws_bytes = pl.sched_off + 256;
+        const size_t counters = sizeof(int) * (1 + (size_t)pl.tail_units * kSoftmaxWarpsMax);
+        pl.ws_bytes = pl.sched_off + ((counters + 255) & ~(size_t)255);
     }
     return pl;
 }
@@ -320,7 +431,9 @@ const char *cpa_status_string(cpa_status s) {
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params) {
     if (validate(batch, params) != CPA_SUCCESS || batch->num_reqs == 0) return 0;
     if (check_attention_support(params) != CPA_SUCCESS) return 0;
-    const Plan pl = make_plan(batch, params);
+    DeviceInfo dev;  // the SM count shapes the plan (tail pieces); none without a device
+    const int sms = device_info(dev) == CPA_SUCCESS ? dev.sms : 0;
+    const Plan pl = make_plan(batch, params, sms);
     return pl.ws_bytes;
 }
 
@@ -373,11 +486,11 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return CPA_ERR_INVALID_ARG;
     if (cpa_status s = check_attention_support(params)) return s;
-    const Plan pl = make_plan(batch, params);
-    const size_t need = pl.ws_bytes;
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CPA_ERR_WORKSPACE;
     DeviceInfo dev;
     if (cpa_status s = device_info(dev)) return s;
+    const Plan pl = make_plan(batch, params, dev.sms);
+    const size_t need = pl.ws_bytes;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CPA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
     const float *q_rscale = nullptr;
@@ -436,6 +549,9 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.interleave = (pl.tile_m == kTcTileM && pl.direct_units > 0 && pl.split_units > 0) ? 1 : 0;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
+    a.tail_units = pl.tail_units;
+    a.tail_pieces = pl.tail_pieces;
+    a.tail_ws = pl.tail_ws_floats;
     a.q = q;
     a.k_new = k_new;
     a.v_new = v_new;
@@ -450,7 +566,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
                                  (params->head_dim * elem_bytes(params) / 16);
         a.write_chunks = (int)((pieces + kWriteChunkPieces - 1) / kWriteChunkPieces);
     }
-    const int units = pl.direct_units + pl.split_units;
+    const int units = attention_units(a);
     // the tensor-core kernel is persistent: at most one CTA per SM, and no
     // more than it has attention units and write pieces
     const int work = units + a.write_chunks;
@@ -469,7 +585,8 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         if (cpa_status s = make_tc_maps(batch, params, q, k_new, v_new, k_cache, v_cache, maps)) return s;
         if (prepass && launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
         a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
-        e = cudaMemsetAsync(a.sched, 0, sizeof(int), st);
+        a.tail_count = pl.tail_units > 0 ? a.sched + 1 : nullptr;
+        e = cudaMemsetAsync(a.sched, 0, sizeof(int) * (1 + (size_t)pl.tail_units * kSoftmaxWarpsMax), st);
         if (e == cudaSuccess) e = launch_attn_tc(a, maps, st);
     } else {
         // the CUDA-core kernel (its pre-pass is RoPE only: FP8 pools need the

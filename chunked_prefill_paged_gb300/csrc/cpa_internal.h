@@ -13,9 +13,15 @@
 //     of "Prefill Processing" (Kernel Interface, Partial KV Segment
 //     Handling) -- each written as a partial (unnormalised output, max,
 //     sum) and merged by attn_merge.
+//   * tail pieces: on the tensor-core kernel, when the direct units would
+//     leave the last wave of CTAs partly idle, the planner may cut each of
+//     the last few direct units (by index) into a few pieces by key tiles.
+//     Each piece writes a partial like a split unit; the CTA that finishes a
+//     unit's last piece merges them into the output, in the same launch.
 // Direct units are numbered first (the heaviest query tiles of each request
-// first), then split units.  Host and device both use request_work() so the
-// launch size and the device-side decode agree.
+// first), the tail pieces in place of the last direct units, then split
+// units.  Host and device both use request_work() so the launch size and the
+// device-side decode agree.
 #pragma once
 
 #include <stdint.h>
@@ -55,6 +61,11 @@ CPA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 // [rows] and sums [rows], padded to a multiple of 4 floats so that every
 // unit's output block starts 16-byte aligned.
 CPA_HD long long partial_floats(int rows, int d) { return (long long)rows * d + ((2 * rows + 3) & ~3); }
+
+// Softmax warps of the tensor-core kernel (counters per tail unit), and the
+// most pieces a tail unit is cut into.
+constexpr int kSoftmaxWarpsMax = 8;
+constexpr int kMaxTailPieces = 4;
 
 struct ReqWork {
     int direct_units;    // H_kv * query tiles, or 0
@@ -103,6 +114,12 @@ struct AttnArgs {
                         // (else kv head innermost); see decode_unit
     int num_direct_units;
     int num_split_units;
+    int tail_units;     // tensor-core kernel, no split units: the last tail_units direct units
+                        // run as tail_pieces pieces each, numbered unit-major in their place
+    int tail_pieces;
+    long long tail_ws;  // float offset in ws of the tail pieces' partials (one per piece)
+    int *tail_count;    // [tail_units * kSoftmaxWarpsMax]: pieces of a unit whose rows of one
+                        // softmax warp are written (zeroed before the launch)
     int interleave;     // tensor-core kernel, batches with both kinds: direct and split units
                         // alternate over the index range (see decode_unit), so that prefill
                         // (tensor-bound) and decode (HBM-bound) units run side by side
@@ -133,6 +150,11 @@ struct AttnArgs {
     const float *v_scale;  // [hkv]
     const float *q_rscale; // [T, hq]
 };
+
+// Work indices of attention (direct units, tail pieces, split units).
+CPA_HD int attention_units(const AttnArgs &a) {
+    return a.num_direct_units + a.num_split_units + a.tail_units * (a.tail_pieces - 1);
+}
 
 // Arguments of the pre-pass over the active tokens' rows: with rotate, turns
 // queries and new keys at absolute position cached[r] + i (pairs (c, c + d/2)

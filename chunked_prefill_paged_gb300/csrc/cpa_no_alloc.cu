@@ -62,10 +62,16 @@ extern "C" cpa_status chunked_prefill_attention_no_alloc(const cpa_batch *batch,
                                                          void *k_cache, void *v_cache, void *out, float *lse,
                                                          void *stream) {
     // 0 for an invalid batch too: chunked_prefill_attention reports that error
-    const size_t need = chunked_prefill_workspace_size(batch, params);
+    cpa_params p = params ? *params : cpa_params{};
+    size_t need = params ? chunked_prefill_workspace_size(batch, &p) : 0;
+    if (need > (size_t)CPA_NO_ALLOC_WORKSPACE_BYTES) {
+        // without tail pieces, whose partials are an optimisation
+        p.flags |= CPA_FLAG_NO_TAIL_SPLIT;
+        need = chunked_prefill_workspace_size(batch, &p);
+    }
     if (need > (size_t)CPA_NO_ALLOC_WORKSPACE_BYTES) return CPA_ERR_WORKSPACE;
     void *ws = no_alloc_workspace();
     if (ws == nullptr) return CPA_ERR_CUDA;
-    return chunked_prefill_attention(batch, params, q, k_new, v_new, k_cache, v_cache, out, lse, ws,
+    return chunked_prefill_attention(batch, params ? &p : nullptr, q, k_new, v_new, k_cache, v_cache, out, lse, ws,
                                      (size_t)CPA_NO_ALLOC_WORKSPACE_BYTES, stream);
 }

@@ -35,7 +35,8 @@ struct Unit {
     int row0, rows;       // packed rows [row0, row0 + rows) of the request (up to
                           // tiles_per_unit * tile_m rows)
     int k_begin, k_end;   // keys [k_begin, k_end) of this unit
-    long long ws_off;     // float offset of the unit's partial (split units)
+    int tail;             // tail piece: index of its direct unit among the tail units, else -1
+    long long ws_off;     // float offset of the unit's partial (split units, tail pieces)
 };
 
 // Decode unit index `unit`; every lane of the calling warp must take part and
@@ -44,6 +45,21 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
     const int lane = threadIdx.x & 31;
     bool split = unit >= a.num_direct_units;
     int target = split ? unit - a.num_direct_units : unit;
+    int tail = -1, tail_piece = 0;
+    if (a.tail_units > 0) {
+        // the last tail_units direct units as tail_pieces pieces each, in their place
+        const int first = a.num_direct_units - a.tail_units;
+        const int pieces_end = first + a.tail_units * a.tail_pieces;
+        if (unit >= first && unit < pieces_end) {
+            tail = (unit - first) / a.tail_pieces;
+            tail_piece = (unit - first) - tail * a.tail_pieces;
+            split = false;
+            target = first + tail;
+        } else if (unit >= pieces_end) {
+            split = true;
+            target = unit - pieces_end;
+        }
+    }
     if (a.interleave && unit < a.num_direct_units + a.num_split_units) {
         // direct (prefill) and split (decode) units spread evenly over the
         // index range, each kind in its own order: index k is direct when
@@ -111,7 +127,20 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
                 const int last_tok = (u.row0 + u.rows - 1) / a.G;
                 u.k_begin = 0;
                 u.k_end = u.C + last_tok + 1;
+                u.tail = tail;
                 u.ws_off = 0;
+                if (tail >= 0) {
+                    // key tiles [j0, j1) of the unit's n (the cached keys in
+                    // tiles from key 0, then the new keys in tiles from key C)
+                    const int nc = cdiv(u.C, kTcTileN);
+                    const int n = nc + cdiv(u.k_end - u.C, kTcTileN);
+                    const int j0 = tail_piece * n / a.tail_pieces, j1 = (tail_piece + 1) * n / a.tail_pieces;
+                    u.piece = tail_piece;
+                    u.k_begin = j0 < nc ? j0 * kTcTileN : u.C + (j0 - nc) * kTcTileN;
+                    if (j1 < n) u.k_end = j1 < nc ? j1 * kTcTileN : u.C + (j1 - nc) * kTcTileN;
+                    u.ws_off = a.tail_ws + ((long long)tail * a.tail_pieces + tail_piece) *
+                                               partial_floats(a.tile_m, a.d);
+                }
             } else {
                 u.qt = 0;
                 u.piece = local / a.hkv;
@@ -119,6 +148,7 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
                 u.rows = rows_total;
                 u.k_begin = u.piece * a.split_len;
                 u.k_end = min(u.k_begin + a.split_len, u.C + u.N);
+                u.tail = -1;
                 u.ws_off = wsb + (long long)local * partial_floats(rows_total, a.d);
             }
             return true;

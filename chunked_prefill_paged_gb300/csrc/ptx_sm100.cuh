@@ -146,6 +146,17 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Add v to a global counter with acquire-release semantics at GPU scope and
+// return the previous value: the caller's earlier writes (and those that a
+// warp or CTA barrier ordered before it) are visible to whoever later
+// acquires the counter, and the caller's later reads see the writes released
+// by earlier adders.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

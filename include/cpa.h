@@ -110,6 +110,9 @@ typedef enum {
 #define CPA_FLAG_FORCE_SIMT 0x2u    /* BF16 only: use the CUDA-core kernel instead of the
                                        tensor-core kernel (cross-checking) */
 #define CPA_FLAG_NO_SPLIT 0x4u      /* never split one query tile's keys across CTAs */
+#define CPA_FLAG_NO_TAIL_SPLIT 0x8u /* tensor-core kernel: never cut the last query tiles of
+                                       a prefill batch into pieces over several CTAs (the
+                                       planner does so when that evens out the last wave) */
 #define CPA_FLAG_TEST_STALL 0x100u  /* testing only: the tensor-core kernel withholds the
                                        copies of one K tile, so its consumers' bounded waits
                                        expire and the launch reports CPA_ERR_DEVICE_TIMEOUT
@@ -165,15 +168,18 @@ typedef struct {
     const float *v_scale;     /* likewise for the values */
 } cpa_params;
 
-/* Bytes of device workspace chunked_prefill_attention needs for this batch:
- * the split-KV partials of the requests that are split (rounded up to 256
- * bytes), the rotated copies of q and k_new when rope_theta > 0 (plain
+/* Bytes of device workspace chunked_prefill_attention needs for this batch
+ * on the current device: the split-KV partials of the requests that are
+ * split, and of the query tiles cut into tail pieces (rounded up to 256
+ * bytes; the tail cut depends on the device's SM count, and there is none
+ * when no device is present), the rotated copies of q and k_new when rope_theta > 0 (plain
  * pools), with the FP8 cache the fp16 copy of q ([T, H_q, d] x 2 bytes), its
  * row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new ([T, H_kv,
  * d] bytes each),
  * and, when the batch runs on the tensor-core kernel (BF16 with
- * num_heads_q / num_heads_kv dividing 128), 256 bytes for that persistent
- * kernel's work counter.  Each part starts on a 256-byte boundary.  0 for an empty batch and for a CUDA-core batch
+ * num_heads_q / num_heads_kv dividing 128), that persistent kernel's work
+ * counter and one counter per softmax warp of every tail-cut tile (4 bytes
+ * each, rounded up to 256 bytes).  Each part starts on a 256-byte boundary.  0 for an empty batch and for a CUDA-core batch
  * with no split.  Reads only host mirrors.  Returns 0 also when the
  * arguments are invalid; chunked_prefill_attention then reports the error. */
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params);

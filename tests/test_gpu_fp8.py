@@ -49,7 +49,7 @@ def as_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_fp8(cpa, w, *, flags=None, rope_theta=0.0, rows_per_req=None, check_pool=True, threads=None):
+def run_fp8(cpa, w, *, flags=None, rope_theta=0.0, rows_per_req=None, rows=None, check_pool=True, threads=None):
     """Every step of `w` over FP8 pools (fused write unless flags say
     otherwise, then the standalone write), against the oracle."""
     sh = w.shape
@@ -79,12 +79,12 @@ def run_fp8(cpa, w, *, flags=None, rope_theta=0.0, rows_per_req=None, check_pool
             qo, kno = to_oracle(q), to_oracle(kn)
         vno = to_oracle(vn) if rope_theta == 0 else as_f64(vn)
         if s.total_new_tokens > 0:
-            rows = None if rows_per_req is None else sample_rows(s, rows_per_req, si)
+            rs = rows if rows is not None else (None if rows_per_req is None else sample_rows(s, rows_per_req, si))
             ref_o, ref_l = oracle.attention(ob, qo, kno, vno, k_pool_o, v_pool_o, num_heads_q=sh.num_heads_q,
                                             num_heads_kv=sh.num_heads_kv, head_dim=sh.head_dim,
-                                            block_size=sh.block_size, scale=sh.scale, rows=rows, threads=threads,
+                                            block_size=sh.block_size, scale=sh.scale, rows=rs, threads=threads,
                                             k_scale=ks, v_scale=vs)
-            idx = slice(None) if rows is None else torch.as_tensor(rows, device=out.device)
+            idx = slice(None) if rs is None else torch.as_tensor(rs, device=out.device)
             res.add(out[idx].float().cpu().numpy(), ref_o, lse[idx].cpu().numpy(), ref_l)
         k_pool_o, v_pool_o = oracle.kv_write(ob, kno, vno, k_pool_o, v_pool_o, num_heads_kv=sh.num_heads_kv,
                                              head_dim=sh.head_dim, block_size=sh.block_size, k_scale=ks, v_scale=vs)
@@ -278,4 +278,16 @@ def test_fp8_speculative_decode_queries(cpa):
     w = W.make_batch_workload("fp8_spec", W.Shape(32, 8, 128, 16, 1024, "bf16"),
                               [(3000, 5), (9000, 5), (17, 5), (12345, 3)], seed=68)
     res = run_fp8(cpa, w)
+    assert_within(res, "bf16")
+
+
+def test_fp8_tail_pieces(cpa):
+    # a prefill chunk whose last query tiles are cut into tail pieces (see
+    # test_gpu_tail.py): every row of the cut tiles, over FP8 pools
+    w = W.make_batch_workload("fp8_tail", W.Shape(32, 8, 128, 128, 1024, "bf16"), [(6144, 2048)], seed=69)
+    b = cpa.Batch(w.steps[0].cached_seq_len, w.steps[0].num_new_tokens, w.block_table)
+    p, _, _ = fp8_params(cpa, w)
+    p_none, _, _ = fp8_params(cpa, w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_NO_TAIL_SPLIT)
+    assert cpa.workspace_size(b, p) > cpa.workspace_size(b, p_none), "no tail cut planned"
+    res = run_fp8(cpa, w, rows=list(range(0, 256)) + [1000, 2047])
     assert_within(res, "bf16")
