@@ -674,6 +674,30 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             } else {
                 // O += P(j) V(j) once the softmax has written P(j)
                 for (int j = 0; j < n; ++j) {
+                    // V(j) first: a partial tile's zeroing then overlaps the
+                    // softmax of tile j
+                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[rs], rph, LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    int key0, valid;
+                    bool pooled;
+                    tl.tile(j, key0, valid, pooled);
+                    if (!F8 && valid < kKT) {
+                        // keys past the tile's valid range: zero their V rows so
+                        // that P = 0 never meets a NaN or Inf left in the pool or
+                        // in this ring slot (eight lanes per 128-byte row, four
+                        // rows at a time; then a proxy fence, as the MMA reads
+                        // through the async proxy)
+                        uint8_t *vs_ = sV + rs * TB + (lane & 7) * 16;
+                        for (int r = valid + (lane >> 3); r < kKT; r += 4) {
+#pragma unroll
+                            for (int h = 0; h < Cfg::kHalves; ++h)
+                                *reinterpret_cast<uint4 *>(vs_ + h * HB + r * 128) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
                     if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.p_full[ub], uph, LIM, abort_flag))) {
                         ok = false;
                         break;
@@ -683,29 +707,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.v_full[rs], rph, LIM, abort_flag))) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
-                    int key0, valid;
-                    bool pooled;
-                    tl.tile(j, key0, valid, pooled);
-                    if (!F8 && valid < kKT) {
-                        // keys past the tile's valid range: zero their V rows so
-                        // that P = 0 never meets a NaN or Inf left in the pool or
-                        // in this ring slot (16 bytes per lane; then a proxy fence,
-                        // as the MMA reads through the async proxy)
-                        uint8_t *vs_ = sV + rs * TB;
-                        const int per_half = (kKT - valid) * 8;  // 16-byte chunks per 64-column half
-                        for (int i = lane; i < per_half * Cfg::kHalves; i += 32) {
-                            const int h = i / per_half, rem = i - h * per_half;
-                            *reinterpret_cast<uint4 *>(vs_ + h * HB + (valid + (rem >> 3)) * 128 + (rem & 7) * 16) =
-                                make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
                     const uint32_t v_lo = v_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
                     const uint32_t tP = tmem + ub * kKT;
 #pragma unroll
