@@ -77,13 +77,16 @@ constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kUnitRing = 4;                // unit indices passed ahead to the other roles
 constexpr int kKConvWarp = 12;              // FP8 cache: warps 12-13 expand K tiles, 14-15 V tiles
+constexpr int kEpiWarp = 12;                // BF16 cache: warps 12-15 write the outputs
 
-// Threads and unit-ring readers of the two kernel flavours: BF16 pools (12
-// warps) and FP8 pools (16 warps: four more expand the codes).
+// Roles of the two kernel flavours (16 warps each): with BF16 pools warps
+// 12-15 take the output epilogue off the softmax warps; with FP8 pools they
+// expand the codes and the softmax warps write the outputs themselves.
 template <bool F8>
 struct TcRoles {
-    static constexpr int kThreads = F8 ? 512 : 384;
-    static constexpr int kUnitReaders = F8 ? 15 : 11;  // every warp but 8 reads every index
+    static constexpr int kThreads = 512;
+    static constexpr int kUnitReaders = 15;  // every warp but 8 reads every index
+    static constexpr bool kEpiWarps = !F8;
 };
 
 template <int D, bool F8>
@@ -110,6 +113,10 @@ struct __align__(8) TcShared {
     uint64_t pv_done[kSBuf];  // per score buffer: the PV that read its P has completed
     uint64_t o_full, o_empty;
     uint64_t mma_done;
+    // BF16 pools: the softmax warps hand each finished unit's row maxima and
+    // sums to the epilogue warps (epi_full), which free the arrays once read
+    uint64_t epi_full, epi_empty;
+    float epi_m[128], epi_l[128];
     uint64_t k8_full[6], v8_full[6];  // FP8 pools: a slot's code tile has landed
     // unit scheduler: warp 8 takes unit indices from the launch's work
     // counter and passes them to the other roles through this ring
@@ -389,7 +396,9 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         }
         for (int b = 0; b < kSBuf; ++b) mbar_init(&sh.pv_done[b], 1);
         mbar_init(&sh.o_full, 1);
-        mbar_init(&sh.o_empty, kSoftmaxThreads);
+        mbar_init(&sh.o_empty, TcRoles<F8>::kEpiWarps ? 128 : kSoftmaxThreads);
+        mbar_init(&sh.epi_full, 8);   // one arrival per softmax warp
+        mbar_init(&sh.epi_empty, 4);  // one per epilogue warp
         mbar_init(&sh.mma_done, 2);  // one commit from each MMA warp
         for (int i = 0; i < kUnitRing; ++i) {
             mbar_init(&sh.unit_full[i], 1);
@@ -737,6 +746,113 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         umma_commit_warp(&sh.mma_done);
         mbar_wait(&sh.mma_done, 0, LIM);
         __syncwarp();
+    } else if (TcRoles<F8>::kEpiWarps && warp >= kEpiWarp) {
+        // =============================================== epilogue (warps 12-15)
+        // Warp 12 + e reads TMEM lanes 32e .. 32e + 31: one thread per output
+        // row with all its D columns.  Per unit: take the rows' maxima and
+        // sums from the softmax warps, wait for the last PV, read O, free it
+        // for the next unit's PVs, and write the rows (a split unit's or tail
+        // piece's partial: unnormalised, with its maxima and sums).
+        const int e = warp - kEpiWarp;
+        const int lr = 32 * e + lane;
+        const uint32_t tO = tmem + ((uint32_t)(32 * e) << 16) + kTmemO;
+        bool ok = true;
+        for (int ec = 0;; ++ec) {
+            Unit u;
+            const int unit = read_unit(sh, ec, LIM, abort_flag, u);
+            if (unit < 0) {
+                ok = false;
+                break;
+            }
+            if (unit >= end_index) break;
+            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
+            const uint32_t ph = (uint32_t)(ec & 1);
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.epi_full, ph, LIM, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const float m = sh.epi_m[lr], l = sh.epi_l[lr];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.epi_empty);
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_full, ph, LIM, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool row_valid = lr < u.rows;
+            const bool warp_rows = __any_sync(0xffffffffu, row_valid);
+            const int pr = u.row0 + lr;  // packed row of the request
+            const int t = u.cu0 + pr / a.G, h = u.g * a.G + pr % a.G;
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int c = 0; c < D / 64 && warp_rows; ++c) {
+                uint32_t r0[32], r1[32];  // output columns 64c .. 64c + 63
+                tmem_ld32(tO + c * 64, r0);
+                tmem_ld32(tO + c * 64 + 32, r1);
+                tmem_wait_ld();
+                if (row_valid) {
+                    if (u.piece >= 0) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.ws + u.ws_off + (long long)lr * D + c * 64);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            dst[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                                                 __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+                            dst[8 + i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
+                                                     __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
+                        }
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                                               ((long long)t * a.hq + h) * D + c * 64);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(r0[8 * i + 0]) * inv, __uint_as_float(r0[8 * i + 1]) * inv);
+                            w.y = pack_bf16(__uint_as_float(r0[8 * i + 2]) * inv, __uint_as_float(r0[8 * i + 3]) * inv);
+                            w.z = pack_bf16(__uint_as_float(r0[8 * i + 4]) * inv, __uint_as_float(r0[8 * i + 5]) * inv);
+                            w.w = pack_bf16(__uint_as_float(r0[8 * i + 6]) * inv, __uint_as_float(r0[8 * i + 7]) * inv);
+                            dst[i] = w;
+                            w.x = pack_bf16(__uint_as_float(r1[8 * i + 0]) * inv, __uint_as_float(r1[8 * i + 1]) * inv);
+                            w.y = pack_bf16(__uint_as_float(r1[8 * i + 2]) * inv, __uint_as_float(r1[8 * i + 3]) * inv);
+                            w.z = pack_bf16(__uint_as_float(r1[8 * i + 4]) * inv, __uint_as_float(r1[8 * i + 5]) * inv);
+                            w.w = pack_bf16(__uint_as_float(r1[8 * i + 6]) * inv, __uint_as_float(r1[8 * i + 7]) * inv);
+                            dst[4 + i] = w;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.o_empty);
+            if (row_valid) {
+                if (u.piece >= 0) {
+                    float *ws = a.ws + u.ws_off;
+                    ws[(long long)u.rows * D + lr] = m;
+                    ws[(long long)u.rows * D + u.rows + lr] = l;
+                } else if (a.lse) {
+                    a.lse[(long long)t * a.hq + h] = (m + __log2f(l)) * 0.69314718055994531f;
+                }
+            }
+            if (u.tail >= 0 && warp_rows) {
+                // a tail piece: the warp that completes the unit's last piece
+                // for its 32 rows (warp 12 + e of every piece's CTA writes
+                // them) merges the pieces' partials of those rows.  The warp
+                // barrier orders the lanes' partial writes before lane 0's
+                // release, and lane 0's acquire before the lanes' reads.
+                __syncwarp();
+                int last = 0;
+                if (lane == 0)
+                    last = atom_add_acq_rel_gpu(a.tail_count + u.tail * kSoftmaxWarpsMax + e, 1) ==
+                           a.tail_pieces - 1;
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __syncwarp();
+                    merge_tail_rows<D>(a, u, 32 * e, lane);
+                    merge_tail_rows<D>(a, u, 32 * e + 16, lane);
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) record_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
     } else if (F8 && warp >= kKConvWarp) {
         // ==================================== FP8 expansion (warps 12-15)
         // Warps 12-13 expand K code tiles, 14-15 V tiles, in their ring slots;
@@ -944,6 +1060,24 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 mbar_arrive(&sh.p_full[b]);
                 prev_b = b;
                 prev_ph = bph;
+            }
+            if (!ok) break;
+            if constexpr (TcRoles<F8>::kEpiWarps) {
+                // the epilogue warps write this unit's rows: hand them each
+                // row's maximum and sum once they have read the previous unit's
+                l += __shfl_xor_sync(0xffffffffu, l, 16);  // whole row
+                if (oc >= 1 && !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.epi_empty, (uint32_t)((oc - 1) & 1),
+                                                                            LIM, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                if (half == 0) {
+                    sh.epi_m[lr] = m_ref;
+                    sh.epi_l[lr] = l;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.epi_full);
+                continue;
             }
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&sh.o_full, (uint32_t)(oc & 1), LIM, abort_flag));
             if (!ok) break;
