@@ -558,11 +558,9 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 return true;
             };
             if (kv_role == 0) {
-                // the first K tile does not depend on the Q buffer: issue it
-                // before waiting for the previous unit's last score MMA
-                ok = load_kv(0, 0);
-                // Q stage it % kQStages; its previous use (unit it - kQStages)
-                // must have finished its last score MMA
+                // Q first: its stage (it % kQStages) was last used two units
+                // ago and is free by now, while the first K tile waits for a
+                // ring slot that the current unit's last score MMAs release
                 constexpr int QS = Cfg::kQStages;
                 const int qb = it % QS;
                 if (ok && it >= QS &&
@@ -576,7 +574,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     if (lane < Cfg::kHalves)
                         tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, u.g * a.G, tok0);
                 }
-                for (int j = 1; j < n && ok; ++j) ok = load_kv(j, 0);
+                for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 0);
                 if (lane == 0) taken = atomicAdd(a.sched, 1);  // this unit's copies are all issued
             } else {
                 for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 1);
@@ -784,14 +782,15 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             const int pr = u.row0 + lr;  // packed row of the request
             const int t = u.cu0 + pr / a.G, h = u.g * a.G + pr % a.G;
             const float inv = 1.f / l;
+            if (u.piece >= 0) {
+                // a partial: the fp32 row goes out before O is freed
 #pragma unroll
-            for (int c = 0; c < D / 64 && warp_rows; ++c) {
-                uint32_t r0[32], r1[32];  // output columns 64c .. 64c + 63
-                tmem_ld32(tO + c * 64, r0);
-                tmem_ld32(tO + c * 64 + 32, r1);
-                tmem_wait_ld();
-                if (row_valid) {
-                    if (u.piece >= 0) {
+                for (int c = 0; c < D / 64 && warp_rows; ++c) {
+                    uint32_t r0[32], r1[32];  // columns 64c .. 64c + 63
+                    tmem_ld32(tO + c * 64, r0);
+                    tmem_ld32(tO + c * 64 + 32, r1);
+                    tmem_wait_ld();
+                    if (row_valid) {
                         float4 *dst = reinterpret_cast<float4 *>(a.ws + u.ws_off + (long long)lr * D + c * 64);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -800,28 +799,34 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                             dst[8 + i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
                                                      __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
                         }
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                                               ((long long)t * a.hq + h) * D + c * 64);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(r0[8 * i + 0]) * inv, __uint_as_float(r0[8 * i + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(r0[8 * i + 2]) * inv, __uint_as_float(r0[8 * i + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(r0[8 * i + 4]) * inv, __uint_as_float(r0[8 * i + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(r0[8 * i + 6]) * inv, __uint_as_float(r0[8 * i + 7]) * inv);
-                            dst[i] = w;
-                            w.x = pack_bf16(__uint_as_float(r1[8 * i + 0]) * inv, __uint_as_float(r1[8 * i + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(r1[8 * i + 2]) * inv, __uint_as_float(r1[8 * i + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(r1[8 * i + 4]) * inv, __uint_as_float(r1[8 * i + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(r1[8 * i + 6]) * inv, __uint_as_float(r1[8 * i + 7]) * inv);
-                            dst[4 + i] = w;
-                        }
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&sh.o_empty);
+            } else {
+                // the row as bf16 in registers (D / 2 words), O freed for the
+                // next unit's PVs, then the stores
+                uint32_t o[D / 2];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];  // columns 32c .. 32c + 31
+                    if (warp_rows) {
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o[16 * c + i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                }
+                tc_fence_before();
+                mbar_arrive(&sh.o_empty);
+                if (row_valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                                           ((long long)t * a.hq + h) * D);
+#pragma unroll
+                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
             }
-            tc_fence_before();
-            mbar_arrive(&sh.o_empty);
             if (row_valid) {
                 if (u.piece >= 0) {
                     float *ws = a.ws + u.ws_off;

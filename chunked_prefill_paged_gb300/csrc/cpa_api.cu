@@ -133,6 +133,9 @@ struct Plan {
     size_t q16_off = 0, qs_off = 0; // FP8 cache: fp16 queries and their row scales
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
+    int split_len_fine = 0;
+    int fine_from = INT32_MAX;  // first request whose pieces are split_len_fine long
+    int fine_units = 0;         // their split units (the launch's last)
     int tail_units = 0;     // the last direct units run as tail_pieces pieces each
     int tail_pieces = 0;
     long long tail_ws_floats = 0;  // float offset of their partials
@@ -266,12 +269,32 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
         if (units < kSplitTargetUnits) break;
         pl.split_len = len;
     }
+    // the persistent kernel's last wave: the last decode requests' keys in
+    // shorter pieces, enough for kFineTailWaves waves of CTAs
+    const int base = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
+    if (tc && sms > 0 && base > 0 && pl.split_len > base) {
+        const int fine = std::max(base, pl.split_len / 4);
+        long long fu = 0;
+        int r1 = b->num_reqs;
+        for (int r = b->num_reqs - 1; r >= 0 && fu < (long long)kFineTailWaves * sms; --r) {
+            fu += request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv, p->head_dim,
+                               pl.tile_m, fine, pl.tiles_per_unit)
+                      .split_units;
+            r1 = r;
+        }
+        if (fu > 0) {
+            pl.fine_from = r1;
+            pl.split_len_fine = fine;
+        }
+    }
     double kv_bytes = 0;
     for (int r = 0; r < b->num_reqs; ++r) {
+        const int len = r >= pl.fine_from ? pl.split_len_fine : pl.split_len;
         const ReqWork w = request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
-                                       p->head_dim, pl.tile_m, pl.split_len, pl.tiles_per_unit);
+                                       p->head_dim, pl.tile_m, len, pl.tiles_per_unit);
         pl.direct_units += w.direct_units;
         pl.split_units += w.split_units;
+        if (r >= pl.fine_from) pl.fine_units += w.split_units;
         pl.split_reqs += w.split_units > 0 ? 1 : 0;
         pl.ws_floats += w.ws_floats;
         kv_bytes += (double)(b->h_cached_seq_len[r] + b->h_num_new_tokens[r]) * p->num_heads_kv * p->head_dim * 2.0 *
@@ -543,10 +566,13 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.num_blocks = params->num_blocks;
     a.scale_log2 = params->scale * 1.4426950408889634f;
     a.split_len = pl.split_len;
+    a.split_len_fine = pl.split_len_fine;
+    a.fine_from = pl.fine_from;
     a.tile_m = pl.tile_m;
     a.tiles_per_unit = pl.tiles_per_unit;
     a.head_major = pl.head_major;
     a.interleave = (pl.tile_m == kTcTileM && pl.direct_units > 0 && pl.split_units > 0) ? 1 : 0;
+    a.interleave_span = pl.direct_units + pl.split_units - pl.fine_units;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
     a.tail_units = pl.tail_units;

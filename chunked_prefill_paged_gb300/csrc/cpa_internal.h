@@ -44,6 +44,11 @@ constexpr int kDefaultSplit = 1024;
 // scheduler to balance -- up to kMaxSplitLen keys per unit.
 constexpr int kSplitTargetUnits = 1024;
 constexpr int kMaxSplitLen = 8192;
+// When the planner lengthened the pieces, the last decode requests (in batch
+// order) take pieces a quarter as long (at least the base length), enough for
+// this many waves of CTAs: their units are the last of the launch, so the
+// last wave ends evenly instead of with some CTAs deep in a long piece.
+constexpr int kFineTailWaves = 3;
 // 16-byte pieces of the new K/V rows per fused-write chunk of the tensor-core
 // kernel (each piece index copies 16 bytes of K and 16 bytes of V)
 constexpr int kWriteChunkPieces = 1024;
@@ -108,6 +113,8 @@ struct AttnArgs {
     int hq, hkv, G, d, bs, num_blocks;
     float scale_log2;  // softmax scale * log2(e)
     int split_len;     // 0: no split units
+    int split_len_fine; // requests fine_from .. num_reqs - 1 cut their keys in pieces of this
+    int fine_from;      // length (the launch's last split units); see split_len_of
     int tile_m;
     int tiles_per_unit; // query tiles per direct unit
     int head_major;     // direct units of a request ordered kv head by kv head
@@ -121,8 +128,10 @@ struct AttnArgs {
     int *tail_count;    // [tail_units * kSoftmaxWarpsMax]: pieces of a unit whose rows of one
                         // softmax warp are written (zeroed before the launch)
     int interleave;     // tensor-core kernel, batches with both kinds: direct and split units
-                        // alternate over the index range (see decode_unit), so that prefill
-                        // (tensor-bound) and decode (HBM-bound) units run side by side
+                        // alternate over indices [0, interleave_span) (see decode_unit), so
+                        // that prefill (tensor-bound) and decode (HBM-bound) units run side
+                        // by side; the split units past the span (the fine ones) come last
+    int interleave_span;
     // data
     const void *q;
     const void *k_new;
@@ -150,6 +159,9 @@ struct AttnArgs {
     const float *v_scale;  // [hkv]
     const float *q_rscale; // [T, hq]
 };
+
+// Piece length of request r's keys when its rows fit one tile.
+CPA_HD int split_len_of(const AttnArgs &a, int r) { return r >= a.fine_from ? a.split_len_fine : a.split_len; }
 
 // Work indices of attention (direct units, tail pieces, split units).
 CPA_HD int attention_units(const AttnArgs &a) {

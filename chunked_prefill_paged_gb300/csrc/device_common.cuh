@@ -60,11 +60,11 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
             target = unit - pieces_end;
         }
     }
-    if (a.interleave && unit < a.num_direct_units + a.num_split_units) {
+    if (a.interleave && unit < a.interleave_span) {
         // direct (prefill) and split (decode) units spread evenly over the
-        // index range, each kind in its own order: index k is direct when
-        // floor((k + 1) D / T) > floor(k D / T), D direct units of T in all
-        const long long D = a.num_direct_units, T = a.num_direct_units + (long long)a.num_split_units;
+        // first T indices, each kind in its own order: index k is direct when
+        // floor((k + 1) D / T) > floor(k D / T); the remaining split units follow
+        const long long D = a.num_direct_units, T = a.interleave_span;
         const long long before = (long long)unit * D / T, after = ((long long)unit + 1) * D / T;
         split = after == before;
         target = split ? (int)(unit - before) : (int)before;
@@ -75,7 +75,7 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
         const int r = r0 + lane;
         ReqWork w{0, 0, 0, 0};
         if (r < a.num_reqs) w = request_work(__ldg(a.cached + r), __ldg(a.nnew + r), a.G, a.hkv, a.d, a.tile_m,
-                                             a.split_len, a.tiles_per_unit);
+                                             split_len_of(a, r), a.tiles_per_unit);
         const int cnt = split ? w.split_units : w.direct_units;
         const long long wsf = split ? w.ws_floats : 0;
         int inc = cnt;
@@ -146,8 +146,9 @@ __device__ __forceinline__ bool decode_unit(const AttnArgs &a, int unit, Unit &u
                 u.piece = local / a.hkv;
                 u.row0 = 0;
                 u.rows = rows_total;
-                u.k_begin = u.piece * a.split_len;
-                u.k_end = min(u.k_begin + a.split_len, u.C + u.N);
+                const int len = split_len_of(a, rr);
+                u.k_begin = u.piece * len;
+                u.k_end = min(u.k_begin + len, u.C + u.N);
                 u.tail = -1;
                 u.ws_off = wsb + (long long)local * partial_floats(rows_total, a.d);
             }

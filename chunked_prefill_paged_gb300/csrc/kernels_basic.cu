@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
             const int rr = r0 + lane;
             ReqWork w{0, 0, 0, 0};
             if (rr < a.num_reqs) w = request_work(__ldg(a.cached + rr), __ldg(a.nnew + rr), a.G, a.hkv, a.d,
-                                                  a.tile_m, a.split_len, a.tiles_per_unit);
+                                                  a.tile_m, split_len_of(a, rr), a.tiles_per_unit);
             const int cnt = w.split_units > 0 ? 1 : 0;
             int inc = cnt;
             long long incw = w.ws_floats;
