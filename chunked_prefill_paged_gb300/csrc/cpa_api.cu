@@ -273,7 +273,7 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     // shorter pieces, enough for kFineTailWaves waves of CTAs
     const int base = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     if (tc && sms > 0 && base > 0 && pl.split_len > base) {
-        const int fine = std::max(base, pl.split_len / 4);
+        const int fine = std::max(base, pl.split_len / 2);
         long long fu = 0;
         int r1 = b->num_reqs;
         for (int r = b->num_reqs - 1; r >= 0 && fu < (long long)kFineTailWaves * sms; --r) {

@@ -45,9 +45,11 @@ constexpr int kDefaultSplit = 1024;
 constexpr int kSplitTargetUnits = 1024;
 constexpr int kMaxSplitLen = 8192;
 // When the planner lengthened the pieces, the last decode requests (in batch
-// order) take pieces a quarter as long (at least the base length), enough for
+// order) take pieces half as long (at least the base length), enough for
 // this many waves of CTAs: their units are the last of the launch, so the
-// last wave ends evenly instead of with some CTAs deep in a long piece.
+// last wave ends evenly instead of with some CTAs deep in a long piece
+// (measured on a 64-decode mixed step: half-length pieces for three waves
+// beat quarter-length ones and four or six waves).
 constexpr int kFineTailWaves = 3;
 // 16-byte pieces of the new K/V rows per fused-write chunk of the tensor-core
 // kernel (each piece index copies 16 bytes of K and 16 bytes of V)
