@@ -67,6 +67,8 @@ CASES = {
     "llama_chunk_fp8": (W.llama3_8b_prompt, -1, 0.0, True),
     "mixed_step_fp8": (W.mixed_step, 0, 0.0, True),
     "speculative_decode_fp8": (W.speculative_decode, 0, 0.0, True),
+    "decode_32x8k": (W.decode_batch, 0, 0.0, False),
+    "decode_32x8k_fp8": (W.decode_batch, 0, 0.0, True),
 }
 
 

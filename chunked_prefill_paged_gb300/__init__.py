@@ -19,7 +19,7 @@ from .binding import (  # noqa: F401
     FLAG_FORCE_SIMT,
     FLAG_FUSE_KV_WRITE,
     FLAG_NO_SPLIT,
-    FLAG_NO_TAIL_SPLIT,
+    FLAG_TAIL_SPLIT,
     FLAG_TEST_STALL,
     KV_FP8_E4M3,
     KV_SAME,

@@ -35,7 +35,7 @@ KV_FP8_E4M3 = 1
 FLAG_FUSE_KV_WRITE = 0x1
 FLAG_FORCE_SIMT = 0x2
 FLAG_NO_SPLIT = 0x4
-FLAG_NO_TAIL_SPLIT = 0x8
+FLAG_TAIL_SPLIT = 0x8
 FLAG_TEST_STALL = 0x100
 
 

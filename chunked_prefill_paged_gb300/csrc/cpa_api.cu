@@ -186,8 +186,8 @@ double schedule_end(FinishHeap h) {
 // p = 2, 3, 4) and keeps the best cut if it ends at least 2% sooner.
 void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
     const int D = pl.direct_units;
-    if (sms <= 0 || D < sms || D > 8 * sms || pl.split_units > 0 ||
-        (p->flags & (CPA_FLAG_NO_SPLIT | CPA_FLAG_NO_TAIL_SPLIT)))
+    if (sms <= 0 || D < sms || D > 8 * sms || pl.split_units > 0 || !(p->flags & CPA_FLAG_TAIL_SPLIT) ||
+        (p->flags & CPA_FLAG_NO_SPLIT))
         return;
     const int G = p->num_heads_q / p->num_heads_kv, hkv = p->num_heads_kv;
     // key tiles of every direct unit in index order (the order decode_unit uses)

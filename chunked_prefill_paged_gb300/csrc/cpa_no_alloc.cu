@@ -66,7 +66,7 @@ extern "C" cpa_status chunked_prefill_attention_no_alloc(const cpa_batch *batch,
     size_t need = params ? chunked_prefill_workspace_size(batch, &p) : 0;
     if (need > (size_t)CPA_NO_ALLOC_WORKSPACE_BYTES) {
         // without tail pieces, whose partials are an optimisation
-        p.flags |= CPA_FLAG_NO_TAIL_SPLIT;
+        p.flags &= ~CPA_FLAG_TAIL_SPLIT;
         need = chunked_prefill_workspace_size(batch, &p);
     }
     if (need > (size_t)CPA_NO_ALLOC_WORKSPACE_BYTES) return CPA_ERR_WORKSPACE;

@@ -110,9 +110,11 @@ typedef enum {
 #define CPA_FLAG_FORCE_SIMT 0x2u    /* BF16 only: use the CUDA-core kernel instead of the
                                        tensor-core kernel (cross-checking) */
 #define CPA_FLAG_NO_SPLIT 0x4u      /* never split one query tile's keys across CTAs */
-#define CPA_FLAG_NO_TAIL_SPLIT 0x8u /* tensor-core kernel: never cut the last query tiles of
-                                       a prefill batch into pieces over several CTAs (the
-                                       planner does so when that evens out the last wave) */
+#define CPA_FLAG_TAIL_SPLIT 0x8u    /* tensor-core kernel, prefill batches: let the planner cut
+                                       the last query tiles into pieces over several CTAs when
+                                       its schedule model expects the last wave to end sooner
+                                       (off by default: with the current kernel it measured no
+                                       faster on 2048-token chunks and slower on long prompts) */
 #define CPA_FLAG_TEST_STALL 0x100u  /* testing only: the tensor-core kernel withholds the
                                        copies of one K tile, so its consumers' bounded waits
                                        expire and the launch reports CPA_ERR_DEVICE_TIMEOUT

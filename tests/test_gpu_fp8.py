@@ -286,8 +286,8 @@ def test_fp8_tail_pieces(cpa):
     # test_gpu_tail.py): every row of the cut tiles, over FP8 pools
     w = W.make_batch_workload("fp8_tail", W.Shape(32, 8, 128, 128, 1024, "bf16"), [(6144, 2048)], seed=69)
     b = cpa.Batch(w.steps[0].cached_seq_len, w.steps[0].num_new_tokens, w.block_table)
-    p, _, _ = fp8_params(cpa, w)
-    p_none, _, _ = fp8_params(cpa, w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_NO_TAIL_SPLIT)
+    p, _, _ = fp8_params(cpa, w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_TAIL_SPLIT)
+    p_none, _, _ = fp8_params(cpa, w)
     assert cpa.workspace_size(b, p) > cpa.workspace_size(b, p_none), "no tail cut planned"
-    res = run_fp8(cpa, w, rows=list(range(0, 256)) + [1000, 2047])
+    res = run_fp8(cpa, w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_TAIL_SPLIT, rows=list(range(0, 256)) + [1000, 2047])
     assert_within(res, "bf16")

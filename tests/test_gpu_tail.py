@@ -1,13 +1,13 @@
-"""Tail pieces on the GPU.  When a prefill batch's query tiles would leave the
-last wave of CTAs partly idle, the planner cuts the last few tiles (by work
-index) into pieces by key tiles; each piece writes a partial (unnormalised
-output, running maximum, sum) and the CTA finishing a tile's last piece
-merges them -- the same online-softmax merge as split decodes ("Prefill
+"""Tail pieces on the GPU.  When a prefill batch's query tiles would leave
+the last wave of CTAs partly idle, the planner (with CPA_FLAG_TAIL_SPLIT)
+cuts the last few tiles (by work index) into pieces by key tiles; each piece
+writes a partial (unnormalised output, running maximum, sum) and the CTA
+finishing a tile's last piece merges them -- the same online-softmax merge as split decodes ("Prefill
 Processing", Partial KV Segment Handling: pieces of one query's keys combine
 to the unsplit result).  Each case checks that the cut is active (the
 workspace grows by the partials), compares every row of the cut tiles and
 a sample of the others with the fp64 oracle, and compares the output with
-the same call under CPA_FLAG_NO_TAIL_SPLIT."""
+the same call without CPA_FLAG_TAIL_SPLIT (the cut is opt-in)."""
 import numpy as np
 import pytest
 import torch
@@ -31,8 +31,8 @@ def run_case(cpa, w, rows):
     t = w.materialize("cuda")
     s = w.steps[0]
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
-    p_tail = params_for(w, flags=0)  # read-only: both calls see the same pool
-    p_none = params_for(w, flags=cpa.FLAG_NO_TAIL_SPLIT)
+    p_tail = params_for(w, flags=cpa.FLAG_TAIL_SPLIT)  # read-only: both calls see the same pool
+    p_none = params_for(w, flags=0)
     assert cpa.workspace_size(b, p_tail) > cpa.workspace_size(b, p_none), "no tail cut planned"
     q, kn, vn = t.step_inputs(s)
     out, lse = cpa.attention(b, p_tail, q, kn, vn, t.k_cache, t.v_cache)

@@ -422,6 +422,15 @@ def speculative_decode(seed: int = 1006, num_reqs: int = 64, drafts: int = 4) ->
                                description=f"{num_reqs} requests x {1 + drafts} tokens over C~U{{1024..32768}}; bs 16")
 
 
+def decode_batch(seed: int = 1007, num_reqs: int = 32, ctx: int = 8192) -> Workload:
+    """Plain decodes (one active token each) over equal contexts; H 32/8,
+    d 128, block 16, kv_segment_size 1024: a small decode-only case (about
+    1 GiB of pool at the defaults) for profiling the split-KV path."""
+    sh = Shape(32, 8, 128, 16, 1024, "bf16")
+    return make_batch_workload(f"decode_{num_reqs}x{ctx}", sh, [(ctx, 1)] * num_reqs, seed, spare=0.1,
+                               description=f"{num_reqs} decodes over {ctx} cached tokens; bs 16")
+
+
 def long_context(seed: int = 1005) -> Workload:
     """70B-shaped GQA: a 32,768-token prompt in 16 chunks of 2048 (last step
     cached 30,720), H_q 64, H_kv 8, d 128, block 16, kv_segment_size 4096,
@@ -438,4 +447,5 @@ ALL = {
     "mixed_step": mixed_step,
     "long_context": long_context,
     "speculative_decode": speculative_decode,
+    "decode_batch": decode_batch,
 }
