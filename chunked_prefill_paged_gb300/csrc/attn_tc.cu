@@ -94,9 +94,14 @@ struct TcCfg {
     static constexpr int kHalves = D / 64;           // 64-element (128 B) column chunks
     static constexpr int kTileBytes = 128 * D * 2;   // 128 rows of D 16-bit values (Q, K or V tile)
     static constexpr int kHalfBytes = kTileBytes / kHalves;
-    static constexpr int kQStages = 2;  // the next unit's Q loads while this one runs
+    // BF16 pools: two Q stages, so the next unit's Q loads while this one
+    // runs.  FP8 pools: one, and a third V stage instead: there a V tile's
+    // slot turns over through its code copy, the expansion and the PV, and
+    // two stages left the PVs waiting (measured: mixed step 1.06 -> 0.99 ms,
+    // 32 decodes 0.226 -> 0.215 ms; a K stage given up instead was slower)
+    static constexpr int kQStages = F8 ? 1 : 2;
     static constexpr int kKStages = (D == 128) ? 3 : 6;
-    static constexpr int kVStages = (D == 128) ? 2 : 5;
+    static constexpr int kVStages = (D == 128) ? (F8 ? 3 : 2) : 5;
     // FP8 pools: a K / V copy brings a code tile (128 rows x D bytes) into the
     // upper half of its ring slot, and the expansion warps turn it in place
     // into the 16-bit tile the MMAs read
