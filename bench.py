@@ -269,7 +269,8 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flops_step = sum(w.flops_per_step())
     # attention, plus the merge kernel when some request is split: the workspace
-    # then holds partials in front of the 256-byte work counter
+    # then holds partials in front of the 256-byte work counter (the bench's
+    # calls use no RoPE, no FP8 and no tail cut, the workspace's other parts)
     launches_per_step = len(w.steps) + sum(1 for b in batches if cpa.workspace_size(b, params) > 256)
 
     def one_step(evs=None):

@@ -381,7 +381,9 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     if (tid == 0) {
         for (int b = 0; b < Cfg::kQStages; ++b) {
             mbar_init(&sh.q_full[b], 1);
-            mbar_init(&sh.q_empty[b], 1);
+            // the last score MMA's commit, and with BF16 pools the four
+            // epilogue warps, which stage the unit's output rows there
+            mbar_init(&sh.q_empty[b], TcRoles<F8>::kEpiWarps ? 1 + 4 : 1);
         }
         // 16-bit tiles: filled by one TMA arrival, or (FP8 pools) by the two
         // expansion warps once the code tile's copies (k8 / v8_full) landed
@@ -825,13 +827,38 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(&sh.o_empty);
-                if (row_valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                                           ((long long)t * a.hq + h) * D);
+                // The stores go through this unit's Q stage, free since its
+                // last score MMA completed (before the softmax could finish
+                // the last tile) and until the warps below release it: each
+                // lane puts its row there (16-byte chunk c of row r at
+                // position (c + r) mod CPR, which spreads a store instruction
+                // over all banks), then every store instruction writes whole
+                // rows (RPI rows of CPR chunks) instead of one chunk of each
+                // of 32 rows.
+                if (warp_rows) {
+                    constexpr int CPR = D / 8;     // 16-byte chunks per row
+                    constexpr int RPI = 32 / CPR;  // rows per store instruction
+                    uint8_t *stage = sQ + (ec % Cfg::kQStages) * TB + e * 32 * (D * 2);
 #pragma unroll
-                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int c = 0; c < CPR; ++c)
+                        *reinterpret_cast<uint4 *>(stage + lane * (D * 2) + (((c + lane) % CPR) << 4)) =
+                            make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    __syncwarp();
+                    const long long row_off = row_valid ? ((long long)t * a.hq + h) * D : -1;
+                    const int c = lane % CPR;
+#pragma unroll 4
+                    for (int i = 0; i < 32 / RPI; ++i) {
+                        const int r = RPI * i + lane / CPR;
+                        const long long off = __shfl_sync(0xffffffffu, row_off, r);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * (D * 2) + (((c + r) % CPR) << 4));
+                        if (off >= 0) reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + off)[c] = v;
+                    }
                 }
             }
+            // the stage's next user is a TMA copy (async proxy)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_empty[ec % Cfg::kQStages]);
             if (row_valid) {
                 if (u.piece >= 0) {
                     float *ws = a.ws + u.ws_off;
