@@ -124,14 +124,32 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     };
     const int h_begin = head_lo + grp * kHeadsPerWarp;
     const int h_end = min(heads, h_begin + kHeadsPerWarp);
-    for (int head = h_begin; head < h_end; ++head) {
+    // every head's elements (and value chunk) are loaded before any is
+    // written: one round of memory latency per warp instead of one per head
+    Lane xls[kHeadsPerWarp], xhs[kHeadsPerWarp];
+    uint4 vvs[kHeadsPerWarp];
+    const bool copy_v = a.write_pool && !a.kv_fp8 && lane < D * (int)sizeof(T) / 16;
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+        const int head = h_begin + i;
+        if (head < h_end) {
+            const bool is_q = head < a.hq;
+            const int hh = is_q ? head : head - a.hq;
+            const long long row = ((long long)t * (is_q ? a.hq : a.hkv) + hh) * D;
+            const T *src = static_cast<const T *>(is_q ? a.q : a.k_new) + row + lane * PPL;
+            xls[i].v = __ldg(reinterpret_cast<const V *>(src));
+            xhs[i].v = __ldg(reinterpret_cast<const V *>(src + HALF));
+            if (!is_q && copy_v) vvs[i] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + row) + lane);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+        const int head = h_begin + i;
+        if (head >= h_end) break;
         const bool is_q = head < a.hq;
         const int hh = is_q ? head : head - a.hq;
         const long long row = ((long long)t * (is_q ? a.hq : a.hkv) + hh) * D;
-        const T *src = static_cast<const T *>(is_q ? a.q : a.k_new) + row + lane * PPL;
-        Lane xl, xh;
-        xl.v = *reinterpret_cast<const V *>(src);
-        xh.v = *reinterpret_cast<const V *>(src + HALF);
+        Lane xl = xls[i], xh = xhs[i];
         if (a.rotate) {
 #pragma unroll
             for (int e = 0; e < PPL; ++e) {
@@ -184,9 +202,7 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
                 *reinterpret_cast<V *>(kp + lane * PPL) = xl.v;
                 *reinterpret_cast<V *>(kp + HALF + lane * PPL) = xh.v;
                 // the value row goes to the same slot unchanged, 16 bytes per lane
-                const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + row);
-                uint4 *vp = reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + prow);
-                for (int c = lane; c < D * (int)sizeof(T) / 16; c += 32) vp[c] = vs[c];
+                if (copy_v) reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + prow)[lane] = vvs[i];
             }
             continue;
         }
