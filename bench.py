@@ -314,36 +314,39 @@ def run_ours(args, rank, world, local):
 
     # end to end through the API with host buffers: H2D of each chunk's
     # q / k / v from pinned memory, the call, D2H of the output.  The copies
-    # run on their own stream, as a serving loop would run them: every
-    # chunk's inputs go up at the start of the step, chunk i's call waits for
-    # its own inputs, and its output comes back while chunk i + 1 computes
-    # (the calls stay in order on the compute stream: each chunk reads the
-    # K/V the previous one wrote).
+    # run on their own streams, one per direction, as a serving loop would
+    # run them: every chunk's inputs go up at the start of the step, chunk
+    # i's call waits for its own inputs, and its output comes back while
+    # chunk i + 1 computes and later inputs still go up (the calls stay in
+    # order on the compute stream: each chunk reads the K/V the previous one
+    # wrote).
     host_in = [tuple(x.cpu().pin_memory() for x in inp) for inp in inputs]
     host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     dev_in = [tuple(torch.empty_like(x) for x in inp) for inp in inputs]
     h2d = sum(x.numel() * x.element_size() for inp in host_in for x in inp)
     d2h = sum(o.numel() * o.element_size() for o in host_out)
-    copy = torch.cuda.Stream(dev)
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in batches]
     ev_done = [torch.cuda.Event() for _ in batches]
 
     def e2e_step():
-        copy.wait_stream(stream)
-        with torch.cuda.stream(copy):
+        copy_in.wait_stream(stream)
+        copy_out.wait_stream(stream)
+        with torch.cuda.stream(copy_in):
             for i, (hin, din) in enumerate(zip(host_in, dev_in)):
                 for d_, h_ in zip(din, hin):
                     d_.copy_(h_, non_blocking=True)
-                ev_in[i].record(copy)
+                ev_in[i].record(copy_in)
         for i, (b, din, o, ho) in enumerate(zip(batches, dev_in, outs, host_out)):
             stream.wait_event(ev_in[i])
             cpa.chunked_prefill_attention(b, params, din[0], din[1], din[2], t.k_cache, t.v_cache, o, None, ws,
                                           stream)
             ev_done[i].record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_done[i])
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(ev_done[i])
                 ho.copy_(o, non_blocking=True)
-        stream.wait_stream(copy)  # the step ends when the last output is on the host
+        stream.wait_stream(copy_in)
+        stream.wait_stream(copy_out)  # the step ends when the last output is on the host
 
     for _ in range(2):
         e2e_step()
