@@ -171,19 +171,23 @@ typedef struct {
 } cpa_params;
 
 /* Bytes of device workspace chunked_prefill_attention needs for this batch
- * on the current device: the split-KV partials of the requests that are
- * split, and of the query tiles cut into tail pieces (rounded up to 256
- * bytes; the tail cut depends on the device's SM count, and there is none
- * when no device is present), the rotated copies of q and k_new when rope_theta > 0 (plain
- * pools), with the FP8 cache the fp16 copy of q ([T, H_q, d] x 2 bytes), its
- * row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new ([T, H_kv,
- * d] bytes each),
- * and, when the batch runs on the tensor-core kernel (BF16 with
- * num_heads_q / num_heads_kv dividing 128), that persistent kernel's work
- * counter and one counter per softmax warp of every tail-cut tile (4 bytes
- * each, rounded up to 256 bytes).  Each part starts on a 256-byte boundary.  0 for an empty batch and for a CUDA-core batch
- * with no split.  Reads only host mirrors.  Returns 0 also when the
- * arguments are invalid; chunked_prefill_attention then reports the error. */
+ * on the current device.  The parts, each starting on a 256-byte boundary:
+ *   - the split-KV partials of the requests whose keys are cut into pieces,
+ *     and (CPA_FLAG_TAIL_SPLIT) of the query tiles cut into tail pieces.
+ *     The plan depends on the device's SM count: how many of the last
+ *     requests take the shorter pieces of the split plan's last wave, and
+ *     the tail cut.  With no device present there is neither;
+ *   - the rotated copies of q and k_new when rope_theta > 0 (plain pools);
+ *   - with the FP8 cache: the fp16 copy of q ([T, H_q, d] x 2 bytes), its row
+ *     scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new
+ *     ([T, H_kv, d] bytes each);
+ *   - when the batch runs on the tensor-core kernel (BF16 with num_heads_q /
+ *     num_heads_kv dividing 128): that persistent kernel's work counter and
+ *     one counter per softmax warp of every tail-cut tile (4 bytes each,
+ *     rounded up to 256 bytes).
+ * 0 for an empty batch and for a CUDA-core batch with no split.  Reads only
+ * host mirrors.  Returns 0 also when the arguments are invalid;
+ * chunked_prefill_attention then reports the error. */
 size_t chunked_prefill_workspace_size(const cpa_batch *batch, const cpa_params *params);
 
 /* Write the K/V rows of every active token into their pool slots: token i of
