@@ -103,8 +103,19 @@ def test_workload_shapes():
     assert sum(lc.pairs_per_step()) == 536887296
 
 
+def test_decode_batch_shape():
+    # the small decode-only profiling case: 32 decodes over 8192 cached
+    # tokens, 513 blocks of 16 each, pool = needed + 10 %
+    w = W.decode_batch()
+    s = w.steps[0]
+    assert w.num_reqs == 32 and s.cached_seq_len.tolist() == [8192] * 32 and s.num_new_tokens.tolist() == [1] * 32
+    need = 32 * W.cdiv(8193, 16)
+    assert w.num_blocks == need + -(-need // 10)
+    assert (w.shape.num_heads_q, w.shape.num_heads_kv, w.shape.head_dim, w.shape.block_size) == (32, 8, 128, 16)
+
+
 def test_block_tables_hold_distinct_physical_blocks():
-    for w in (W.llama3_8b_prompt(), W.mixed_step(), W.long_context()):
+    for w in (W.llama3_8b_prompt(), W.mixed_step(), W.long_context(), W.decode_batch()):
         used = []
         for r in range(w.num_reqs):
             last = w.steps[-1]
