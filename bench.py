@@ -91,6 +91,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: seconds of oracle work over the whole run (warm-up included)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--case", choices=sorted(CASES) + ["serving"], default=None,
@@ -567,7 +569,7 @@ def run_reference(args, rank, world):
     t = w.materialize("cpu", sentinel=W.SENTINEL_ZERO)
     t_cpu = {"q": to_oracle_np(t.q), "k": to_oracle_np(t.k), "v": to_oracle_np(t.v),
              "k_cache": to_oracle_np(t.k_cache), "v_cache": to_oracle_np(t.v_cache)}
-    per = max(2.0, 60.0 / max(args.steps + args.warmup, 1))
+    per = max(1.0, getattr(args, "ref_seconds", 60.0) / max(args.steps + args.warmup, 1))
     vals = []
     desc = ""
     cores = 1
@@ -579,9 +581,12 @@ def run_reference(args, rank, world):
     wall = time.perf_counter() - t0
     value = statistics.mean(vals) if vals else 0.0
     sh = w.shape
+    # the time a whole step (all five chunks) takes at the sampled rate
+    ms_step = sum(w.flops_per_step()) / (value * 1e12) * 1e3 if value > 0 else None
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 1) if ms_step else None, "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "H_q": sh.num_heads_q,
                    "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim, "block_size": sh.block_size},
