@@ -1,0 +1,159 @@
+"""The library's host-side work planner (make_plan in csrc/cpa_api.cu) on the
+CPU, through tests/plan_harness.cu, which compiles the planner with stub
+launchers and runs it for a given SM count.  A GPU is needed for the planner
+to see an SM count in the library itself (workspace sizes on a machine with no
+device carry no SM-dependent part), so these cases pin the SM-dependent
+choices here:
+
+* the split length grows from kv_segment_size while the batch keeps at least
+  1024 units, up to 8192 keys;
+* the fine tail: the last requests in batch order whose split units, at half
+  the piece length, make three waves of CTAs;
+* the interleave span: prefill and decode units alternate over the indices
+  before the fine tail's units;
+* the opt-in tail cut of prefill batches (CPA_FLAG_TAIL_SPLIT);
+* the workspace layout (partials, then the counters, 256-byte aligned).
+
+The expected values restate the rules in plain Python over the same inputs."""
+import json
+import math
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FUSE, NO_SPLIT, TAIL_SPLIT = 0x1, 0x4, 0x8
+
+
+@pytest.fixture(scope="module")
+def harness(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc is not available")
+    exe = str(tmp_path_factory.mktemp("plan") / "plan_harness")
+    subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                    os.path.join(ROOT, "tests", "plan_harness.cu"), "-o", exe], check=True, capture_output=True)
+    return exe
+
+
+def plan(harness, reqs, sms=152, hq=32, hkv=8, d=128, bs=16, seg=1024, flags=FUSE, kv_format=0):
+    text = f"{sms} {hq} {hkv} {d} {bs} {seg} 1 {flags} {kv_format} {len(reqs)}\n"
+    text += "\n".join(f"{c} {n}" for c, n in reqs) + "\n"
+    out = subprocess.run([harness], input=text, capture_output=True, text=True, check=True).stdout
+    return json.loads(out)
+
+
+def split_pieces(C, N, G, length):
+    """Pieces of a request whose rows fit one 128-row tile, else 0 (a direct request)."""
+    if N <= 0 or math.ceil(N * G / 128) > 1:
+        return 0
+    k = math.ceil((C + N) / length)
+    return k if k > 1 else 0
+
+
+def direct_units(C, N, G, hkv, length):
+    return 0 if N <= 0 or split_pieces(C, N, G, length) else hkv * math.ceil(N * G / 128)
+
+
+def expected(reqs, sms, G=4, hkv=8, base=1024):
+    length = base
+    while length * 2 <= 8192:
+        units = sum(hkv * split_pieces(c, n, G, length * 2) + direct_units(c, n, G, hkv, length * 2)
+                    for c, n in reqs)
+        if units < 1024:
+            break
+        length *= 2
+    fine_from, fine = -1, 0
+    if sms > 0 and length > base:
+        fine = max(base, length // 2)
+        fu = 0
+        r1 = len(reqs)
+        for r in range(len(reqs) - 1, -1, -1):
+            if fu >= 3 * sms:
+                break
+            fu += hkv * split_pieces(*reqs[r], G, fine)
+            r1 = r
+        if fu > 0:
+            fine_from = r1
+        else:
+            fine = 0
+    lens = [fine if fine_from >= 0 and r >= fine_from else length for r in range(len(reqs))]
+    split = [hkv * split_pieces(c, n, G, l) for (c, n), l in zip(reqs, lens)]
+    direct = [direct_units(c, n, G, hkv, l) for (c, n), l in zip(reqs, lens)]
+    fine_units = sum(split[r] for r in range(len(reqs)) if fine_from >= 0 and r >= fine_from)
+    return dict(split_len=length, split_len_fine=fine if fine_from >= 0 else 0, fine_from=fine_from,
+                fine_units=fine_units, split_units=sum(split), direct_units=sum(direct),
+                interleave_span=sum(split) + sum(direct) - fine_units)
+
+
+def check(got, want):
+    for k, v in want.items():
+        assert got[k] == v, (k, got[k], v)
+
+
+@pytest.mark.parametrize("sms", [152, 64, 0])
+def test_decode_batch_plan(harness, sms):
+    reqs = [(8192, 1)] * 32
+    got = plan(harness, reqs, sms=sms)
+    want = expected(reqs, sms)
+    check(got, want)
+    if sms == 152:
+        # 32 x 5 pieces of 2048 keys; the last 7 requests (9 pieces of 1024
+        # each, 72 units apiece, 504 >= 3 x 152) form the fine tail
+        assert (got["split_len"], got["split_len_fine"], got["fine_from"], got["fine_units"]) == (2048, 1024, 25, 504)
+    if sms == 0:
+        assert got["fine_from"] == -1 and got["split_units"] == 32 * 5 * 8
+    # partials (4 rows x 128 + 8 floats per piece and head), then one 256-byte counter block
+    floats = got["split_units"] * (4 * 128 + 8)
+    assert got["sched_off"] == math.ceil(floats * 4 / 256) * 256
+    assert got["ws_bytes"] == got["sched_off"] + 256
+
+
+def test_mixed_step_plan_interleaves_before_the_fine_tail(harness):
+    w = W.mixed_step()
+    s = w.steps[0]
+    reqs = [(int(c), int(n)) for c, n in zip(s.cached_seq_len, s.num_new_tokens)]
+    got = plan(harness, reqs)
+    check(got, expected(reqs, 152))
+    # the fine tail is the last decodes; the prefill chunks (after them in
+    # batch order) stay direct, and every direct unit precedes the fine tail
+    n_dec = sum(1 for _, n in reqs if n == 1)
+    assert 0 <= got["fine_from"] < n_dec
+    assert got["fine_units"] >= 3 * 152
+    assert got["direct_units"] <= got["interleave_span"] < got["direct_units"] + got["split_units"]
+
+
+def test_no_split_flag_keeps_every_request_direct(harness):
+    reqs = [(8192, 1)] * 32
+    got = plan(harness, reqs, flags=FUSE | NO_SPLIT)
+    assert got["split_units"] == 0 and got["direct_units"] == 32 * 8 and got["fine_from"] == -1
+    assert got["ws_bytes"] == 256  # the work counter only
+
+
+@pytest.mark.parametrize("flags,sms,cut", [(FUSE | TAIL_SPLIT, 152, (56, 2)), (FUSE, 152, (0, 0)),
+                                          (FUSE | TAIL_SPLIT, 0, (0, 0)),
+                                          (FUSE | TAIL_SPLIT | NO_SPLIT, 152, (0, 0))])
+def test_tail_cut_is_opt_in(harness, flags, sms, cut):
+    # a 2048-token chunk over 6144 cached tokens: 512 query tiles of about
+    # 56 key tiles, 3.37 waves on 152 SMs; with the flag the planner cuts
+    # the last wave's 56 tiles in two
+    got = plan(harness, [(6144, 2048)], sms=sms, bs=128, flags=flags)
+    assert got["direct_units"] == 512 and got["split_units"] == 0
+    assert (got["tail_units"], got["tail_pieces"]) == cut
+    # partials of the pieces (128 rows x 128 + 256 floats each), then the
+    # work counter and eight counters per cut tile
+    floats = cut[0] * cut[1] * (128 * 128 + 256)
+    counters = math.ceil(4 * (1 + 8 * cut[0]) / 256) * 256
+    assert got["ws_bytes"] == math.ceil(floats * 4 / 256) * 256 + counters
+
+
+def test_fp8_pools_plan_like_bf16(harness):
+    reqs = [(8192, 1)] * 32
+    bf16 = plan(harness, reqs)
+    fp8 = plan(harness, reqs, kv_format=1)
+    for k in ("split_len", "split_len_fine", "fine_from", "split_units", "direct_units"):
+        assert fp8[k] == bf16[k]
