@@ -44,6 +44,7 @@ MUT_ROPE_NO_OFFSET = 10
 MUT_FP8_NEW_UNQUANTIZED = 11
 MUT_FP8_HEAD0_SCALE = 12
 MUT_FP8_TRUNCATE = 13
+MUT_SEES_NEXT_KEY = 14
 
 
 class _Problem(ctypes.Structure):

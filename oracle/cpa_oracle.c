@@ -114,6 +114,7 @@ enum {
     MUT_FP8_NEW_UNQUANTIZED = 11, /* FP8 cache: the active tokens' own keys/values skip the cache format */
     MUT_FP8_HEAD0_SCALE = 12,  /* FP8 cache: every kv head uses head 0's scales */
     MUT_FP8_TRUNCATE = 13,     /* FP8 encoder truncates instead of rounding to nearest */
+    MUT_SEES_NEXT_KEY = 14,    /* causal limit one too far: token also sees the key after its own */
 };
 
 /* Value of an FP8 E4M3 code (NaN for S.1111.111). */
@@ -222,6 +223,7 @@ static int make_row(const orc_problem *P, int t, int h, row_info *ri) {
     int p = (P->mutation == MUT_NO_POSITION_OFFSET) ? ri->i : C + ri->i;
     ri->first_key = (P->mutation == MUT_DROP_CACHED) ? C : 0;
     ri->last_key = (P->mutation == MUT_DROP_DIAGONAL) ? p - 1 : p;
+    if (P->mutation == MUT_SEES_NEXT_KEY && p + 1 < C + P->num_new_tokens[r]) ri->last_key = p + 1;
     if (ri->last_key < ri->first_key) ri->last_key = ri->first_key; /* keep >= 1 key */
     return 0;
 }

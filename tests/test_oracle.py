@@ -327,7 +327,7 @@ def test_pins_pass_on_the_unmodified_oracle():
 @pytest.mark.parametrize("mutation", [oracle.MUT_DROP_DIAGONAL, oracle.MUT_GQA_MODULO,
                                       oracle.MUT_NO_POSITION_OFFSET, oracle.MUT_DROP_CACHED,
                                       oracle.MUT_NO_BLOCK_TABLE, oracle.MUT_NO_SCALE,
-                                      oracle.MUT_MERGE_NO_RESCALE])
+                                      oracle.MUT_MERGE_NO_RESCALE, oracle.MUT_SEES_NEXT_KEY])
 def test_planted_attention_mistake_is_caught(mutation):
     assert not _pins_pass(mutation=mutation)
 
