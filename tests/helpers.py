@@ -15,7 +15,14 @@ BF16_ATOL = 2e-2   # max-abs error bound for BF16 outputs against the fp64 oracl
 FP32_ATOL = 1e-4   # max-abs error bound for FP32 outputs
 BF16_LSE_ATOL = 2e-3
 FP32_LSE_ATOL = 1e-4
-BF16_REL_RMS = 1e-2  # diagnostic gate on relative RMS error
+BF16_REL_RMS = 1e-2  # gate on the relative RMS error of each checked step
+# Gate on every (token, query head) row: |o_gpu - o_ref|_2 <= ROW_REL * |o_ref|_2.
+# BF16 output rounding alone gives about 2^-9 / sqrt(3) relative per row, and
+# P rounded to bf16 before the PV product about as much again; a mask or
+# offset error confined to one row moves that row by far more once the
+# softmax is peaked (the peaky and needle input variants).
+BF16_ROW_REL = 2e-2
+FP32_ROW_REL = 1e-3
 
 
 def to_oracle(t: torch.Tensor) -> np.ndarray:
@@ -64,6 +71,7 @@ class Result:
         self.max_err = 0.0
         self.max_lse_err = 0.0
         self.rel_rms = []
+        self.max_row_rel = 0.0
         self.rows_checked = 0
 
     def add(self, gpu_out: np.ndarray, ref_out: np.ndarray, gpu_lse: Optional[np.ndarray], ref_lse: np.ndarray):
@@ -72,6 +80,9 @@ class Result:
         self.max_err = max(self.max_err, float(err.max()) if err.size else 0.0)
         if err.size:
             self.rel_rms.append(float(np.sqrt((err ** 2).mean()) / max(np.sqrt((ref_out ** 2).mean()), 1e-30)))
+            e_row = np.sqrt((err ** 2).sum(axis=-1))
+            r_row = np.sqrt((ref_out.astype(np.float64) ** 2).sum(axis=-1))
+            self.max_row_rel = max(self.max_row_rel, float((e_row / np.maximum(r_row, 1e-30)).max()))
         if gpu_lse is not None and gpu_lse.size:
             self.max_lse_err = max(self.max_lse_err, float(np.abs(gpu_lse.astype(np.float64) - ref_lse).max()))
         self.rows_checked += gpu_out.shape[0]
@@ -79,13 +90,15 @@ class Result:
 
 def run_and_compare(w: W.Workload, *, flags=None, kv_segment_size=None, rows_per_req: Optional[int] = None,
                     steps_to_check: Optional[Sequence[int]] = None, threads=None, check_pool=True,
-                    seed: int = 0, device="cuda"):
+                    seed: int = 0, device="cuda", variant: str = "plain"):
     """Run every step of `w` on the GPU (fused K/V write unless flags say
     otherwise, then the standalone write) and in the oracle; compare the
-    checked steps' outputs (all rows, or a sample) and the final pool."""
+    checked steps' outputs (all rows, or a sample) and the final pool.
+    variant: the query values (workloads.apply_variant)."""
     import chunked_prefill_paged_gb300 as cpa
     sh = w.shape
     t = w.materialize(device)
+    W.apply_variant(t, variant, sh.num_heads_q // sh.num_heads_kv)
     k_pool_o = to_oracle(t.k_cache)
     v_pool_o = to_oracle(t.v_cache)
     params = params_for(w, flags, kv_segment_size)
@@ -120,11 +133,24 @@ def run_and_compare(w: W.Workload, *, flags=None, kv_segment_size=None, rows_per
     return res
 
 
-def assert_within(res: Result, dtype: str):
+def gate_failures(res: Result, dtype: str) -> List[str]:
+    """The gates every parity test applies, as a list of the ones that fail."""
+    bad = []
     if dtype == "f32":
-        assert res.max_err <= FP32_ATOL, f"max-abs error {res.max_err:.3e} > {FP32_ATOL}"
-        assert res.max_lse_err <= FP32_LSE_ATOL, f"lse error {res.max_lse_err:.3e}"
+        atol, lse_tol, row_tol = FP32_ATOL, FP32_LSE_ATOL, FP32_ROW_REL
     else:
-        assert res.max_err <= BF16_ATOL, f"max-abs error {res.max_err:.3e} > {BF16_ATOL}"
-        assert res.max_lse_err <= BF16_LSE_ATOL, f"lse error {res.max_lse_err:.3e}"
-        assert max(res.rel_rms) <= BF16_REL_RMS, f"relative RMS error {max(res.rel_rms):.3e}"
+        atol, lse_tol, row_tol = BF16_ATOL, BF16_LSE_ATOL, BF16_ROW_REL
+    if not res.max_err <= atol:
+        bad.append(f"max-abs error {res.max_err:.3e} > {atol}")
+    if not res.max_lse_err <= lse_tol:
+        bad.append(f"lse error {res.max_lse_err:.3e} > {lse_tol}")
+    if not res.max_row_rel <= row_tol:
+        bad.append(f"row relative error {res.max_row_rel:.3e} > {row_tol}")
+    if dtype != "f32" and res.rel_rms and not max(res.rel_rms) <= BF16_REL_RMS:
+        bad.append(f"relative RMS error {max(res.rel_rms):.3e} > {BF16_REL_RMS}")
+    return bad
+
+
+def assert_within(res: Result, dtype: str):
+    bad = gate_failures(res, dtype)
+    assert not bad, "; ".join(bad)

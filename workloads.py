@@ -202,6 +202,41 @@ class Tensors:
         return self.q[idx].contiguous(), self.k[idx].contiguous(), self.v[idx].contiguous()
 
 
+VARIANTS = ("plain", "peaky", "needle")
+
+
+def apply_variant(t: Tensors, variant: str, group: int) -> None:
+    """Reshape the query values of materialized inputs, in place, so that a
+    parity check cannot pass on a wrong mask.
+
+    plain   N(0, 1) queries as drawn.  Over thousands of keys the softmax is
+            nearly flat and outputs are about 0.01-0.05 in size.
+    peaky   queries times 4 (a power of two: exact in bf16 and fp32); scores
+            then have a standard deviation of about 4, a few keys carry most
+            of the weight and outputs are O(1).
+    needle  query row t of every query head is the sum of value row t's key
+            and value row t + 1's key (of the kv head that serves that query
+            head, heads grouped contiguously: kv head h // group), rounded to
+            the element type.  In a prompt, value row t + 1 is the next
+            position, so a row's own key and the key just past its causal
+            limit both score about sqrt(d) above the rest: the output is
+            dominated by the row's own value row, and a mask that drops the
+            diagonal or lets the next key in changes it by O(1).
+    """
+    if variant == "plain":
+        return
+    if variant == "peaky":
+        t.q.mul_(4)
+        return
+    if variant != "needle":
+        raise ValueError(f"unknown variant {variant!r}")
+    k = t.k.float()
+    nxt = torch.zeros_like(k)
+    nxt[:-1] = k[1:]
+    src = (k + nxt).repeat_interleave(group, dim=1)  # [rows, H_q, d]
+    t.q.copy_(src.to(t.q.dtype))
+
+
 def _gen(device: torch.device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
