@@ -370,10 +370,14 @@ def run_ours(args, rank, world, local):
                 "kernel": "attn_tc_kernel<128, false>",
                 "algorithmic_flops_per_launch": flops_step / len(w.steps)}
 
-    secondary = fp8_mixed = None
+    host_copies = pinned_copy_rates(dev, h2d, d2h, e2e_ms / args.steps)
+
+    secondary = fp8_mixed = prefix = long_last = None
     if not args.no_secondary:
         secondary = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush)
         fp8_mixed = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=True)
+        prefix = run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, W.prefix_cache, 0)
+        long_last = run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, W.long_context, -1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -386,20 +390,114 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "chunks_per_step": len(w.steps),
-                   "H_q": sh.num_heads_q, "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim,
-                   "block_size": sh.block_size, "kv_segment_size": sh.kv_segment_size,
-                   "flops_per_step": flops_step, "l2": "flushed before every timed step (256 MiB write)",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(w, world),
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "host_copies": host_copies,
         "secondary": secondary,
         "fp8_mixed": fp8_mixed,
+        "prefix_cache": prefix,
+        "long_context_last": long_last,
     }
     return line
+
+
+def pinned_copy_rates(dev, h2d_bytes, d2h_bytes, e2e_ms_per_step):
+    """Plain pinned-host copy rates on this machine, one cudaMemcpyAsync per
+    direction of the e2e leg's byte counts (H2D alone, D2H alone, both at
+    once on two streams), beside the rate the e2e leg's copies reach."""
+    up_h = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    up_d = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dn_d = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    dn_h = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=10):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            up_d.copy_(up_h, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            dn_h.copy_(dn_d, non_blocking=True)
+
+    def both():
+        up()
+        down()
+
+    t_up, t_dn, t_both = timed(up), timed(down), timed(both)
+    gbs = lambda b, t: round(b / t / 1e9, 1)
+    return {"h2d_gbs": gbs(h2d_bytes, t_up), "d2h_gbs": gbs(d2h_bytes, t_dn),
+            "both_gbs": gbs(h2d_bytes + d2h_bytes, t_both),
+            "e2e_leg_gbs": gbs(h2d_bytes + d2h_bytes, e2e_ms_per_step / 1e3),
+            "e2e_leg_frac_of_both": round(t_both / (e2e_ms_per_step / 1e3), 3),
+            "how": "one pinned cudaMemcpyAsync per direction of the e2e bytes, host wall time over 10 reps"}
+
+
+def warm_cache(cpa, w, t, params, dev, upto):
+    """Write the K/V of steps [0, upto) into the pool (as the earlier chunks'
+    calls would have), so a later chunk reads real cached values."""
+    for s in w.steps[:upto]:
+        b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
+        _, k, v = t.step_inputs(s)
+        cpa.paged_kv_write(b, params, k, v, t.k_cache, t.v_cache)
+
+
+def run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, make, idx):
+    """A prefill-heavy configuration's attention call (one workload step,
+    its cache holding the earlier chunks' K/V): algorithmic TFLOP/s against
+    the measured bf16 peak."""
+    import chunked_prefill_paged_gb300 as cpa
+    w = make()
+    sh = w.shape
+    t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
+    i = idx % len(w.steps)
+    s = w.steps[i]
+    params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    warm_cache(cpa, w, t, params, dev, i)
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
+    q, k, v = t.step_inputs(s)
+    out = torch.empty_like(q)
+    n = cpa.workspace_size(b, params)
+    ws = torch.empty(max(n // 4, 4), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError(f"device error in {w.name}")
+    ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
+    flops = w.flops_per_step()[i]
+    achieved = flops / (ms / 1e3) / 1e12
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "step": i, "cached_seq_len": [int(x) for x in sorted(set(s.cached_seq_len))],
+            "tokens": int(s.total_new_tokens), "metric": "chunk-attn TFLOP/s (algorithmic, visible pairs only)",
+            "value": round(achieved, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "flops_per_step": flops,
+            "launches_per_step": 1,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
+                         "traffic": None, "kernel": "attn_tc_kernel<128, false>"},
+            "l2": "flushed before every timed call (256 MiB write)"}
 
 
 def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=False):
@@ -462,6 +560,7 @@ def run_case(args, local):
                         cpa.FLAG_FUSE_KV_WRITE, rope_theta=rope_theta)
     if fp8:
         fp8_inputs(cpa, w, t, params, dev)
+    warm_cache(cpa, w, t, params, dev, idx % len(w.steps))
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
     q, k, v = t.step_inputs(s)
     out = torch.empty_like(q)
@@ -560,9 +659,22 @@ def run_serving(args, local):
                        "system_prompts": "4 x 1024 tokens", "suffix": "U{128..1024}", "max_new_tokens": max_new}}
 
 
+def bench_config(w: W.Workload, world: int) -> dict:
+    """The bench line's config (both arms print the same one)."""
+    sh = w.shape
+    return {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "chunks_per_step": len(w.steps),
+            "H_q": sh.num_heads_q, "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim,
+            "block_size": sh.block_size, "kv_segment_size": sh.kv_segment_size,
+            "flops_per_step": sum(w.flops_per_step()), "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
-    """The oracle as it stands on the host cores, same metric and workload;
-    each step a bounded sample."""
+    """The oracle as it stands on the host cores, same metric and workload.
+    Each step is a bounded sample of the workload (query rows of the last
+    chunk, all heads); value is the algorithmic TFLOP/s of the sampled work,
+    ms_per_step the wall time each sampled step took.  The time a whole step
+    (all five chunks) would take at that rate is reported separately."""
     if rank != 0:
         return None
     w = W.llama3_8b_prompt()
@@ -570,29 +682,28 @@ def run_reference(args, rank, world):
     t_cpu = {"q": to_oracle_np(t.q), "k": to_oracle_np(t.k), "v": to_oracle_np(t.v),
              "k_cache": to_oracle_np(t.k_cache), "v_cache": to_oracle_np(t.v_cache)}
     per = max(1.0, getattr(args, "ref_seconds", 60.0) / max(args.steps + args.warmup, 1))
-    vals = []
+    vals, walls = [], []
     desc = ""
     cores = 1
-    t0 = time.perf_counter()
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         v_, cores, desc = oracle_sample(w, t_cpu, per)
         if i >= args.warmup:
             vals.append(v_)
-    wall = time.perf_counter() - t0
+            walls.append(time.perf_counter() - t0)
     value = statistics.mean(vals) if vals else 0.0
-    sh = w.shape
-    # the time a whole step (all five chunks) takes at the sampled rate
-    ms_step = sum(w.flops_per_step()) / (value * 1e12) * 1e3 if value > 0 else None
+    ms_sample = 1e3 * statistics.mean(walls) if walls else None
+    full_ms = sum(w.flops_per_step()) / (value * 1e12) * 1e3 if value > 0 else None
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 1) if ms_step else None, "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "prompt_tokens": 10000, "chunk": 2048, "H_q": sh.num_heads_q,
-                   "H_kv": sh.num_heads_kv, "head_dim": sh.head_dim, "block_size": sh.block_size},
+        "warmup": args.warmup, "ms_per_step": round(ms_sample, 1) if ms_sample else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": bench_config(w, world),
+        "step_kind": "a bounded sample of the workload per step (see cpu_baseline.sample); "
+                     "ms_per_step is the wall time of that sample, including its cache set-up",
+        "ms_per_full_step_extrapolated": round(full_ms, 1) if full_ms else None,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "wall_s": round(wall, 1),
     }
 
 

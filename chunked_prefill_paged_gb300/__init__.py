@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     KV_FP8_E4M3,
     KV_SAME,
     LIB_PATH,
+    NO_ALLOC_WORKSPACE_BYTES,
     SUCCESS,
     Batch,
     CpaError,

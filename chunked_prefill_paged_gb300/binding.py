@@ -37,6 +37,8 @@ FLAG_FORCE_SIMT = 0x2
 FLAG_NO_SPLIT = 0x4
 FLAG_TAIL_SPLIT = 0x8
 FLAG_TEST_STALL = 0x100
+# bytes of the static device array behind chunked_prefill_attention_no_alloc
+NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
 class CpaError(RuntimeError):

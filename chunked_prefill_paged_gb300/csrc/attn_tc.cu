@@ -57,6 +57,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "launch.h"
 #include "ptx_sm100.cuh"
@@ -1199,15 +1201,20 @@ template <int D, bool F8>
 cudaError_t launch_tc(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_t stream) {
     constexpr int smem = TcCfg<D, F8>::kSmemBytes;
     // set once per device (a repeated set is harmless), so that later calls
-    // make no attribute call and can be captured into a CUDA graph
+    // make no attribute call and can be captured into a CUDA graph; host
+    // threads launching at once take the lock
+    static std::mutex attr_mutex;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(attr_mutex);
+        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+            e = cudaFuncSetAttribute(attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        }
     }
     attn_tc_kernel<D, F8><<<grid, TcRoles<F8>::kThreads, smem, stream>>>(a, m.q, m.k_new, m.v_new, m.k_pool,
                                                                           m.v_pool);

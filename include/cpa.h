@@ -230,18 +230,27 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
  * workspace -- a plugin inside a host application that owns all device memory
  * through its own pool, or a serving loop that must not call cudaMalloc /
  * cudaFree because they can synchronise the device.  This call takes the same
- * arguments minus the workspace and allocates nothing: the split-KV partials
- * go to one file-scope device array of CPA_NO_ALLOC_WORKSPACE_BYTES that every
- * GPU loading the library holds until the process exits.
- *   - A batch whose partials need more than that (see
- *     chunked_prefill_workspace_size) returns CPA_ERR_WORKSPACE and launches
- *     nothing.
+ * arguments minus the workspace and allocates nothing: the whole workspace
+ * that chunked_prefill_workspace_size reports -- split-KV and tail-piece
+ * partials, the RoPE / FP8 pre-pass copies of the active rows, the work and
+ * tail counters -- goes to one file-scope device array of
+ * CPA_NO_ALLOC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * the process exits.  The pre-pass copies grow with the active tokens, so
+ * RoPE and FP8 batches reach the limit at fewer tokens than plain ones.
+ *   - With CPA_FLAG_TAIL_SPLIT, a batch whose workspace does not fit is run
+ *     without tail pieces (as if the flag were clear: the same result up to
+ *     the order of fp32 sums).  A batch that does not fit without them
+ *     returns CPA_ERR_WORKSPACE and launches nothing.
  *   - All calls on a device share the array, which keeps the last call's
- *     contents; nothing in it has to start at zero.  Calls that overlap on the
- *     GPU (e.g. on two streams at once) race on it: serialise them.
+ *     contents; the call clears the counters itself (an asynchronous memset
+ *     on `stream`) and writes every partial before reading it.  Calls that
+ *     overlap on the GPU (e.g. on two streams at once) race on it: serialise
+ *     them.
  *   - The first call on a device looks up the array's device address and
- *     caches it; make that first call before any stream capture.
- * Results are those of chunked_prefill_attention on the same inputs. */
+ *     caches it; make that first call before any stream capture.  After
+ *     cudaDeviceReset the cached addresses are stale: reload the library.
+ * Results are bit-identical to chunked_prefill_attention's on the same
+ * inputs and flags (whenever the tail pieces fit). */
 cpa_status chunked_prefill_attention_no_alloc(const cpa_batch *batch, const cpa_params *params,
                                               const void *q, const void *k_new, const void *v_new,
                                               void *k_cache, void *v_cache, void *out, float *lse,
@@ -250,7 +259,9 @@ cpa_status chunked_prefill_attention_no_alloc(const cpa_batch *batch, const cpa_
 /* Wait for `stream`, then return and clear the first error recorded by a
  * kernel on the current device since the last call (CPA_SUCCESS if none):
  * CPA_ERR_DEVICE_TIMEOUT or CPA_ERR_BAD_BLOCK_ID.  CPA_ERR_CUDA if the
- * stream itself reports an error.  This call synchronises the stream. */
+ * stream itself reports an error.  This call synchronises the stream.  The
+ * library caches the error word's device address per device on first use;
+ * after cudaDeviceReset that address is stale: reload the library. */
 cpa_status cpa_last_device_error(void *stream);
 
 /* Static description of a status code. */

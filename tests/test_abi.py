@@ -40,6 +40,12 @@ def test_every_declared_function_is_exported(lib):
     assert set(lib.EXPORTED) <= names
 
 
+def test_binding_constants_match_the_header(lib):
+    text = open(os.path.join(ROOT, "include", "cpa.h")).read()
+    m = re.search(r"#define CPA_NO_ALLOC_WORKSPACE_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == lib.NO_ALLOC_WORKSPACE_BYTES
+
+
 def test_version_and_status_strings(lib):
     L = lib.load()
     assert L.cpa_version() >= 100
