@@ -179,7 +179,8 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-KERNEL_SOURCES = ("attn_tc.cu", "device_common.cuh", "ptx_sm100.cuh", "cpa_internal.h", "cpa_api.cu")
+KERNEL_SOURCES = ("attn_tc2.cu", "attn_tc.cu", "tc_common.cuh", "device_common.cuh", "ptx_sm100.cuh",
+                  "cpa_internal.h", "cpa_api.cu")
 
 
 def kernel_sources_sha256() -> str:

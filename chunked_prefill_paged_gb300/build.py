@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcpa.so")
-SOURCES = ["cpa_api.cu", "kernels_basic.cu", "attn_tc.cu", "cpa_no_alloc.cu", "engine.cpp"]
+SOURCES = ["cpa_api.cu", "kernels_basic.cu", "attn_tc.cu", "attn_tc2.cu", "cpa_no_alloc.cu", "engine.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -62,22 +62,22 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "ptx_sm100.cuh"
+#include "tc_common.cuh"
 
 namespace cpa {
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;      // Q and K copies
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;    // V copies
 constexpr int kPvWarp = 11;           // PV MMA issuer
-constexpr int kKT = kTcTileN;         // keys per K/V tile (128)
 constexpr int kSBuf = 3;              // score buffers in TMEM
 constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kUnitRing = 4;                // unit indices passed ahead to the other roles
 constexpr int kKConvWarp = 12;              // FP8 cache: warps 12-13 expand K tiles, 14-15 V tiles
 constexpr int kEpiWarp = 12;                // BF16 cache: warps 12-15 write the outputs
 
@@ -127,57 +127,9 @@ struct __align__(8) TcShared {
     uint64_t k8_full[6], v8_full[6];  // FP8 pools: a slot's code tile has landed
     // unit scheduler: warp 8 takes unit indices from the launch's work
     // counter and passes them to the other roles through this ring
-    uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
-    int unit_ring[kUnitRing];
-    Unit unit_desc[kUnitRing];  // the decoded unit of each ring slot
+    UnitRing ring;
     uint32_t tmem_base;
     int abort_flag;
-};
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Key tiles of a unit: the cached part [k_begin, min(k_end, C)) then the new
-// part [max(k_begin, C), k_end), each cut into 128-key tiles.
-struct TileList {
-    int n_cached, n_total;
-    int cached_end, new_begin;
-    int k_begin, k_end;
-    __device__ __forceinline__ void init(const Unit &u) {
-        k_begin = u.k_begin;
-        k_end = u.k_end;
-        cached_end = min(u.k_end, u.C);
-        new_begin = max(u.k_begin, u.C);
-        n_cached = cached_end > k_begin ? cdiv(cached_end - k_begin, kKT) : 0;
-        const int nn = k_end > new_begin ? cdiv(k_end - new_begin, kKT) : 0;
-        n_total = n_cached + nn;
-    }
-    // first key of tile j, keys valid in it, and whether it comes from the pool
-    __device__ __forceinline__ void tile(int j, int &key0, int &valid, bool &pooled) const {
-        if (j < n_cached) {
-            key0 = k_begin + j * kKT;
-            valid = min(kKT, cached_end - key0);
-            pooled = true;
-        } else {
-            key0 = new_begin + (j - n_cached) * kKT;
-            valid = min(kKT, k_end - key0);
-            pooled = false;
-        }
-    }
 };
 
 // Four E4M3 codes (bytes of w, lowest address first) as fp16 pairs: codes
@@ -321,39 +273,6 @@ __device__ __forceinline__ void merge_tail_rows(const AttnArgs &a, const Unit &u
     }
 }
 
-// A decoded unit through a ring slot: the scheduling warp decodes each unit
-// once, as soon as it has claimed it, and every other role copies the fields
-// (the slot's mbarrier orders the stores before the loads).
-__device__ __forceinline__ void put_unit(Unit &dst, const Unit &u) {
-    volatile int *d = reinterpret_cast<volatile int *>(&dst);
-    const int *v = reinterpret_cast<const int *>(&u);
-#pragma unroll
-    for (int k = 0; k < (int)(sizeof(Unit) / 4); ++k) d[k] = v[k];
-}
-__device__ __forceinline__ void get_unit(Unit &u, const Unit &src) {
-    const volatile int *d = reinterpret_cast<const volatile int *>(&src);
-    int *v = reinterpret_cast<int *>(&u);
-#pragma unroll
-    for (int k = 0; k < (int)(sizeof(Unit) / 4); ++k) v[k] = d[k];
-}
-
-// The i-th unit of this CTA, as published by the scheduling warp (every lane
-// of the calling warp takes part): its index, and for an attention unit its
-// decoded fields in u.  The index is >= the unit count for a piece of the K/V
-// write or when the CTA is done; -1 when the wait gave up (timeout or abort).
-__device__ __forceinline__ int read_unit(TcShared &sh, int i, long long limit, const volatile int *abort_flag,
-                                         Unit &u) {
-    const int s = i % kUnitRing;
-    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.unit_full[s], (uint32_t)((i / kUnitRing) & 1), limit,
-                                                    abort_flag)))
-        return -1;
-    const int unit = *reinterpret_cast<volatile int *>(&sh.unit_ring[s]);
-    get_unit(u, sh.unit_desc[s]);
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.unit_empty[s]);
-    return unit;
-}
-
 template <int D, bool F8>
 __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -410,8 +329,8 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         mbar_init(&sh.epi_empty, 4);  // one per epilogue warp
         mbar_init(&sh.mma_done, 2);  // one commit from each MMA warp
         for (int i = 0; i < kUnitRing; ++i) {
-            mbar_init(&sh.unit_full[i], 1);
-            mbar_init(&sh.unit_empty[i], TcRoles<F8>::kUnitReaders);
+            mbar_init(&sh.ring.full[i], 1);
+            mbar_init(&sh.ring.empty[i], TcRoles<F8>::kUnitReaders);
         }
         sh.abort_flag = 0;
         fence_mbar_init();
@@ -460,21 +379,19 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 unit = __shfl_sync(0xffffffffu, taken, 0);
                 const int s = it % kUnitRing;
                 if (it >= kUnitRing &&
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.unit_empty[s],
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.ring.empty[s],
                                                                 (uint32_t)((it / kUnitRing - 1) & 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
                 if (unit < total_units) decode_unit(a, unit, u);  // once, for every role
                 if (lane == 0) {
-                    put_unit(sh.unit_desc[s], u);
-                    sh.unit_ring[s] = unit;
-                    mbar_arrive(&sh.unit_full[s]);  // release: index and fields are visible to every waiter
+                    publish_unit(sh.ring, it, unit, u);
                     // pieces of the K/V write need no copies: claim the next index now
                     if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
                 }
             } else {
-                unit = read_unit(sh, it, LIM, abort_flag, u);
+                unit = read_unit(sh.ring, it, LIM, abort_flag, u);
                 if (unit < 0) {
                     ok = false;
                     break;
@@ -635,7 +552,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         const bool s_role = (warp == kMmaWarp);
         for (int ucnt = 0;; ++ucnt) {  // ucnt: units started
             Unit u;
-            const int unit = read_unit(sh, ucnt, LIM, abort_flag, u);
+            const int unit = read_unit(sh.ring, ucnt, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -766,7 +683,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         bool ok = true;
         for (int ec = 0;; ++ec) {
             Unit u;
-            const int unit = read_unit(sh, ec, LIM, abort_flag, u);
+            const int unit = read_unit(sh.ring, ec, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -907,7 +824,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         bool ok = true;
         for (int cc = 0;; ++cc) {
             Unit u;
-            const int unit = read_unit(sh, cc, LIM, abort_flag, u);
+            const int unit = read_unit(sh.ring, cc, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
@@ -957,7 +874,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         bool ok = true;
         for (int oc = 0;; ++oc) {  // oc: units started
             Unit u;
-            const int unit = read_unit(sh, oc, LIM, abort_flag, u);
+            const int unit = read_unit(sh.ring, oc, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;

@@ -125,6 +125,7 @@ bool use_tensor_cores(const cpa_params *p) {
 
 struct Plan {
     int tile_m = 0;
+    bool tc2 = false;        // the two-pipeline tensor-core kernel (attn_tc2.cu)
     int tiles_per_unit = 1;
     int head_major = 0;
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
@@ -250,13 +251,69 @@ void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
     }
 }
 
+// Query tiles per direct unit for the two-pipeline kernel on a batch of
+// direct units only: pairs, whose K/V tiles serve 256 rows, or single tiles
+// split by keys over the two pipelines.  Both do the same tensor work; pairs
+// halve the K/V copies (and TMA boxes) per FLOP, single tiles make twice as
+// many units, which can fill the launch's last wave of CTAs better.  A greedy
+// list schedule of the units (the work counter's order: requests in turn,
+// each request's heaviest query tiles first, kv heads innermost) on `sms`
+// CTAs, with costs in periods of 1024 cycles -- a key tile costs a pair 2
+// periods and a single tile 1, or the TMA issue time of its K and V boxes
+// (about 75 cycles a box) when that is longer, plus a switch of 4 periods per
+// unit -- picks the one that ends sooner (pairs unless singles end 3 %
+// sooner).  Batches with split units keep pairs.
+constexpr double kBoxCycles = 75.0;
+constexpr double kUnitSwitchPeriods = 4.0;
+
+int choose_tiles_per_unit(const cpa_batch *b, const cpa_params *p, int sms, const Plan &pl) {
+    if (sms <= 0 || pl.split_units > 0 || pl.direct_units == 0) return 2;
+    const int G = p->num_heads_q / p->num_heads_kv, hkv = p->num_heads_kv;
+    const int bs = std::min(p->block_size, kTcTileN);
+    const double boxes = 2.0 * cdiv(kTcTileN, bs) * (p->head_dim / 64) * kBoxCycles / 1024.0;
+    auto end_time = [&](int tpu) {
+        FinishHeap h;
+        for (int c = 0; c < sms; ++c) h.push(0.0);
+        for (int r = 0; r < b->num_reqs; ++r) {
+            const int C = b->h_cached_seq_len[r], N = b->h_num_new_tokens[r];
+            if (N <= 0) continue;
+            const int rows = N * G, n_qt = cdiv(rows, kTcTileM), groups = cdiv(n_qt, tpu);
+            for (int i = 0; i < groups; ++i) {
+                const int last = n_qt - 1 - i * tpu, first = std::max(0, last - tpu + 1);
+                const int last_tok = (std::min((last + 1) * kTcTileM, rows) - 1) / G;
+                const int n = cdiv(C, kTcTileN) + cdiv(last_tok + 1, kTcTileN);
+                const double per_tile = last > first ? std::max(2.0, boxes) : std::max(1.0, boxes);
+                const double cost = n * per_tile + kUnitSwitchPeriods;
+                for (int g = 0; g < hkv; ++g) {
+                    const double f = h.top() + cost;
+                    h.pop();
+                    h.push(f);
+                }
+            }
+        }
+        return schedule_end(h);
+    };
+    return end_time(1) < 0.97 * end_time(2) ? 1 : 2;
+}
+
 Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     Plan pl;
     const bool tc = use_tensor_cores(p);
     pl.tile_m = tc ? kTcTileM : kSimtTileM;
-    pl.tiles_per_unit = 1;
-    pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
+    // The two-pipeline kernel (attn_tc2.cu) runs BF16 batches at block sizes
+    // 16 and 32 that have query tiles to pair: a 128-key tile there takes 16
+    // or 8 TMA boxes per operand, and pairs halve the boxes per FLOP.  The
+    // one-pipeline kernel (attn_tc.cu) runs the rest -- block sizes 64 and
+    // 128, decode-only batches (both measured faster on it), FP8 pools and
+    // the opt-in tail cut.  Pairs unless a batch of direct units only
+    // schedules better with single tiles (choose_tiles_per_unit, below).
     const int G = p->num_heads_q / p->num_heads_kv;
+    bool pairs = false;
+    for (int r = 0; r < b->num_reqs && !pairs; ++r)
+        pairs = (long long)b->h_num_new_tokens[r] * G > kTcTileM;
+    pl.tc2 = tc && !kv_fp8(p) && !(p->flags & CPA_FLAG_TAIL_SPLIT) && p->block_size <= 32 && pairs;
+    pl.tiles_per_unit = pl.tc2 ? 2 : 1;
+    pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     // fewer, longer split units while the batch keeps enough of them: every
     // unit costs a switch (its lookups, the epilogue, the pipeline's refill)
     for (int len = pl.split_len * 2; pl.split_len > 0 && len <= kMaxSplitLen; len *= 2) {
@@ -303,6 +360,14 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     // K/V of the batch larger than about half of L2: walk the direct units
     // head by head so that concurrent CTAs share K/V tiles in L2
     pl.head_major = kv_bytes > kHeadMajorKvBytes ? 1 : 0;
+    if (pl.tc2 && choose_tiles_per_unit(b, p, sms, pl) == 1) {
+        pl.tiles_per_unit = 1;
+        pl.direct_units = 0;
+        for (int r = 0; r < b->num_reqs; ++r)
+            pl.direct_units += request_work(b->h_cached_seq_len[r], b->h_num_new_tokens[r], G, p->num_heads_kv,
+                                            p->head_dim, pl.tile_m, pl.split_len, 1)
+                                   .direct_units;
+    }
     if (tc) plan_tail(b, p, sms, pl);
     if (pl.tail_units > 0) {
         pl.tail_ws_floats = pl.ws_floats;
@@ -613,7 +678,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
         a.tail_count = pl.tail_units > 0 ? a.sched + 1 : nullptr;
         e = cudaMemsetAsync(a.sched, 0, sizeof(int) * (1 + (size_t)pl.tail_units * kSoftmaxWarpsMax), st);
-        if (e == cudaSuccess) e = launch_attn_tc(a, maps, st);
+        if (e == cudaSuccess) e = pl.tc2 ? launch_attn_tc2(a, maps, st) : launch_attn_tc(a, maps, st);
     } else {
         // the CUDA-core kernel (its pre-pass is RoPE only: FP8 pools need the
         // tensor-core kernel)

@@ -23,5 +23,7 @@ cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t stream);
 cudaError_t launch_attn_merge(const AttnArgs &a, int dtype, int num_split_reqs, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs &a, const TcMaps &maps, cudaStream_t stream);
+// two query tiles per unit (a.tiles_per_unit == 2), BF16 pools (attn_tc2.cu)
+cudaError_t launch_attn_tc2(const AttnArgs &a, const TcMaps &maps, cudaStream_t stream);
 
 }  // namespace cpa

@@ -16,6 +16,7 @@ cudaError_t launch_rope(const RopeArgs &, int, cudaStream_t) { return cudaErrorN
 cudaError_t launch_attn_simt(const AttnArgs &, int, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_attn_merge(const AttnArgs &, int, int, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_attn_tc(const AttnArgs &, const TcMaps &, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_attn_tc2(const AttnArgs &, const TcMaps &, cudaStream_t) { return cudaErrorNotSupported; }
 }  // namespace cpa
 
 int main() {
@@ -50,9 +51,10 @@ int main() {
     const cpa::Plan pl = cpa::make_plan(&b, &p, sms);
     printf("{\"split_len\": %d, \"split_len_fine\": %d, \"fine_from\": %d, \"fine_units\": %d, "
            "\"direct_units\": %d, \"split_units\": %d, \"split_reqs\": %d, \"tail_units\": %d, \"tail_pieces\": %d, "
-           "\"head_major\": %d, \"interleave_span\": %d, \"ws_bytes\": %zu, \"sched_off\": %zu}\n",
+           "\"head_major\": %d, \"interleave_span\": %d, \"ws_bytes\": %zu, \"sched_off\": %zu, "
+           "\"tiles_per_unit\": %d, \"tc2\": %d}\n",
            pl.split_len, pl.split_len_fine, pl.fine_from == INT32_MAX ? -1 : pl.fine_from, pl.fine_units,
            pl.direct_units, pl.split_units, pl.split_reqs, pl.tail_units, pl.tail_pieces, pl.head_major,
-           pl.direct_units + pl.split_units - pl.fine_units, pl.ws_bytes, pl.sched_off);
+           pl.direct_units + pl.split_units - pl.fine_units, pl.ws_bytes, pl.sched_off, pl.tiles_per_unit, pl.tc2 ? 1 : 0);
     return 0;
 }

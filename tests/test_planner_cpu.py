@@ -12,7 +12,11 @@ choices here:
 * the interleave span: prefill and decode units alternate over the indices
   before the fine tail's units;
 * the opt-in tail cut of prefill batches (CPA_FLAG_TAIL_SPLIT);
-* the workspace layout (partials, then the counters, 256-byte aligned).
+* the workspace layout (partials, then the counters, 256-byte aligned);
+* the kernel and the query tiles per direct unit: the two-pipeline kernel
+  for BF16 batches at block sizes 16 and 32 with query tiles to pair, with
+  pairs unless single tiles schedule better; else the one-pipeline kernel
+  with single tiles.
 
 The expected values restate the rules in plain Python over the same inputs."""
 import json
@@ -55,14 +59,16 @@ def split_pieces(C, N, G, length):
     return k if k > 1 else 0
 
 
-def direct_units(C, N, G, hkv, length):
-    return 0 if N <= 0 or split_pieces(C, N, G, length) else hkv * math.ceil(N * G / 128)
+def direct_units(C, N, G, hkv, length, tiles_per_unit=2):
+    if N <= 0 or split_pieces(C, N, G, length):
+        return 0
+    return hkv * math.ceil(math.ceil(N * G / 128) / tiles_per_unit)
 
 
-def expected(reqs, sms, G=4, hkv=8, base=1024):
+def expected(reqs, sms, G=4, hkv=8, base=1024, tiles_per_unit=2):
     length = base
     while length * 2 <= 8192:
-        units = sum(hkv * split_pieces(c, n, G, length * 2) + direct_units(c, n, G, hkv, length * 2)
+        units = sum(hkv * split_pieces(c, n, G, length * 2) + direct_units(c, n, G, hkv, length * 2, tiles_per_unit)
                     for c, n in reqs)
         if units < 1024:
             break
@@ -83,7 +89,7 @@ def expected(reqs, sms, G=4, hkv=8, base=1024):
             fine = 0
     lens = [fine if fine_from >= 0 and r >= fine_from else length for r in range(len(reqs))]
     split = [hkv * split_pieces(c, n, G, l) for (c, n), l in zip(reqs, lens)]
-    direct = [direct_units(c, n, G, hkv, l) for (c, n), l in zip(reqs, lens)]
+    direct = [direct_units(c, n, G, hkv, l, tiles_per_unit) for (c, n), l in zip(reqs, lens)]
     fine_units = sum(split[r] for r in range(len(reqs)) if fine_from >= 0 and r >= fine_from)
     return dict(split_len=length, split_len_fine=fine if fine_from >= 0 else 0, fine_from=fine_from,
                 fine_units=fine_units, split_units=sum(split), direct_units=sum(direct),
@@ -142,6 +148,8 @@ def test_tail_cut_is_opt_in(harness, flags, sms, cut):
     # 56 key tiles, 3.37 waves on 152 SMs; with the flag the planner cuts
     # the last wave's 56 tiles in two
     got = plan(harness, [(6144, 2048)], sms=sms, bs=128, flags=flags)
+    # block size 128: the one-pipeline kernel, single query tiles
+    assert (got["tc2"], got["tiles_per_unit"]) == (0, 1)
     assert got["direct_units"] == 512 and got["split_units"] == 0
     assert (got["tail_units"], got["tail_pieces"]) == cut
     # partials of the pieces (128 rows x 128 + 256 floats each), then the
@@ -157,3 +165,68 @@ def test_fp8_pools_plan_like_bf16(harness):
     fp8 = plan(harness, reqs, kv_format=1)
     for k in ("split_len", "split_len_fine", "fine_from", "split_units", "direct_units"):
         assert fp8[k] == bf16[k]
+
+
+def test_query_tile_pairs_with_bf16_pools_only(harness):
+    # a 2048-token chunk: 64 query tiles per kv head, in 32 pairs with BF16
+    # pools; FP8 pools keep single tiles (their kernel has one tile per unit)
+    bf16 = plan(harness, [(4096, 2048)], bs=16)
+    fp8 = plan(harness, [(4096, 2048)], bs=16, kv_format=1)
+    assert (bf16["tiles_per_unit"], bf16["direct_units"]) == (2, 8 * 32)
+    assert (fp8["tiles_per_unit"], fp8["direct_units"]) == (1, 8 * 64)
+    # an odd tile count: the last pair of each head is a single tile
+    odd = plan(harness, [(0, 3 * 32)], bs=16)
+    assert odd["direct_units"] == 8 * 2
+
+
+def expected_tiles_per_unit(reqs, sms, G=4, hkv=8, bs=16, d=128):
+    """The planner's choice restated: the two-pipeline kernel only at block
+    sizes 16 and 32 with some request of more than 128 rows (else single
+    tiles on the one-pipeline kernel); there, greedy list schedules of
+    pairs and of single query tiles (costs in 1024-cycle periods: a key tile
+    max(2, boxes) for a pair, max(1, boxes) for a single tile, boxes = K and
+    V TMA boxes x 75 cycles; 4 per unit); singles when they end 3 % sooner."""
+    import heapq
+    if bs > 32 or not any(n * G > 128 for _, n in reqs):
+        return 1
+    boxes = 2 * math.ceil(128 / min(bs, 128)) * (d // 64) * 75 / 1024
+
+    def end(tpu):
+        h = [0.0] * sms
+        for c, n_tok in reqs:
+            if n_tok <= 0:
+                continue
+            rows = n_tok * G
+            n_qt = math.ceil(rows / 128)
+            for i in range(math.ceil(n_qt / tpu)):
+                last = n_qt - 1 - i * tpu
+                first = max(0, last - tpu + 1)
+                last_tok = (min((last + 1) * 128, rows) - 1) // G
+                n = math.ceil(c / 128) + math.ceil((last_tok + 1) / 128)
+                cost = n * (max(2, boxes) if last > first else max(1, boxes)) + 4
+                for _ in range(hkv):
+                    heapq.heappush(h, heapq.heappop(h) + cost)
+        return max(h)
+
+    return 1 if end(1) < 0.97 * end(2) else 2
+
+
+@pytest.mark.parametrize("reqs,bs,hq", [([(8192, 1808)], 128, 32), ([(8192, 1808)], 16, 64),
+                                        ([(6144, 2048)], 128, 32), ([(0, 2048)], 128, 32),
+                                        ([(4096, 300), (4096, 512), (100, 1000)], 16, 32),
+                                        ([(30720, 2048)], 16, 64), ([(2048, 700), (0, 64)], 64, 32)])
+def test_tiles_per_unit_choice(harness, reqs, bs, hq):
+    got = plan(harness, reqs, bs=bs, hq=hq)
+    want = expected_tiles_per_unit(reqs, 152, G=hq // 8, bs=bs)
+    assert got["tiles_per_unit"] == want
+    assert got["direct_units"] == sum(direct_units(c, n, hq // 8, 8, 1024, want) for c, n in reqs)
+
+
+def test_kernel_choice(harness):
+    # block size 16 with rows to pair: the two-pipeline kernel
+    assert plan(harness, [(30720, 2048)], bs=16, hq=64)["tc2"] == 1
+    # block size 128, decode-only batches, FP8 pools, the tail cut: one pipeline
+    assert plan(harness, [(8192, 1808)], bs=128)["tc2"] == 0
+    assert plan(harness, [(8192, 1)] * 8, bs=16)["tc2"] == 0
+    assert plan(harness, [(30720, 2048)], bs=16, kv_format=1)["tc2"] == 0
+    assert plan(harness, [(30720, 2048)], bs=16, flags=FUSE | TAIL_SPLIT)["tc2"] == 0
