@@ -75,11 +75,11 @@ constexpr int kReaders2 = 15;          // every warp but 8 reads every unit
 constexpr float kRescaleThreshold2 = 8.0f;  // log2 units
 // Registers per thread: the launch gives 128 to each of the 512 threads; the
 // two softmax warpgroups take 184 (a row's 128 scores stay in registers),
-// warps 8-11 keep 80 and the epilogue warpgroup 64 (2 x 184 + 80 + 64 =
+// warps 8-11 keep 88 and the epilogue warpgroup 56 (2 x 184 + 88 + 56 =
 // 4 x 128; a split that compiles without spills).
 constexpr uint32_t kRegsSoftmax = 184;
-constexpr uint32_t kRegsOther = 80;
-constexpr uint32_t kRegsEpilogue = 64;
+constexpr uint32_t kRegsOther = 88;
+constexpr uint32_t kRegsEpilogue = 56;
 constexpr int kLaunchRegs = 128;
 
 template <int D>
@@ -101,7 +101,6 @@ struct __align__(8) Tc2Shared {
     uint64_t v_ready[4];             // a V tile may be read: landed, partial rows zeroed
     uint64_t s_full[2];              // per query tile: S_X(j) is in TMEM
     uint64_t p_full[2];              // P_X(j) written (one arrival per softmax warp of X)
-    uint64_t pv_done[2];             // PV_X(j) has completed
     uint64_t o_full[2], o_empty[2];  // a unit's O_X complete / read by the epilogue
     uint64_t epi_full, epi_empty;    // row maxima and sums handed to the epilogue
     uint64_t mma_done;
@@ -177,7 +176,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mbar_init(&sh.q_empty[x], 1);
             mbar_init(&sh.s_full[x], 1);
             mbar_init(&sh.p_full[x], 4);  // the four softmax warps of the tile
-            mbar_init(&sh.pv_done[x], 1);
             mbar_init(&sh.o_full[x], 1);
             mbar_init(&sh.o_empty[x], 4);  // the four epilogue warps
         }
@@ -466,11 +464,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
                 umma_commit_warp(&sh.s_full[x]);
             };
-            // O_X += P_X(j) V(j) once the softmax has written P_X(j)
-            auto issue_pv = [&](int x, int j, uint32_t vt, uint32_t &pv_cnt, uint32_t o_use) -> bool {
+            const TileList *tl_cur = nullptr;  // the unit being issued (for the V tiles' valid keys)
+            // O_X += P_X(j) V(vt) once the softmax has written P_X(j).  The
+            // first PV to read a V tile waits for it: for a full tile until it
+            // has landed, for a partial one until its rows past the valid keys
+            // are zeroed too (which the V producer does after it has landed).
+            auto issue_pv = [&](int x, int j, uint32_t vt, int vtile, bool first, uint32_t &pv_cnt,
+                                uint32_t o_use) -> bool {
                 const int vs = (int)(vt % NSV);
-                if (!wait(&sh.v_ready[vs], (vt / NSV) & 1u)) return false;
-                if (!wait(&sh.v_full[vs], (vt / NSV) & 1u)) return false;
+                if (first) {
+                    int key0, valid;
+                    bool pooled;
+                    tl_cur->tile(vtile, key0, valid, pooled);
+                    if (!wait(valid < kKT ? &sh.v_ready[vs] : &sh.v_full[vs], (vt / NSV) & 1u)) return false;
+                }
                 if (j == 0 && o_use >= 1 && !wait(&sh.o_empty[x], (o_use - 1) & 1u)) return false;
                 if (!wait(&sh.p_full[x], pv_cnt & 1u)) return false;
                 tc_fence_after();
@@ -481,7 +488,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 for (int kk = 0; kk < kKT / 16; ++kk)
                     umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
                                   (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit_warp(&sh.pv_done[x]);
                 ++pv_cnt;
                 return true;
             };
@@ -497,6 +503,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
                 TileList tl;
                 tl.init(u);
+                tl_cur = &tl;
                 const int n = tl.n_total;
                 const UnitShape us = unit_shape(a, u, tl);
                 const bool ks = us.key_split;
@@ -520,7 +527,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     // PV_B(j - 1): tile B is the last reader of its V tile
                     if (j >= 1 && j - 1 < us.nt1) {
                         const uint32_t vt = v_it + key_tile(1, j - 1);
-                        if (!issue_pv(1, j - 1, vt, pv_cnt_b, o_use_b)) break;
+                        if (!issue_pv(1, j - 1, vt, (int)key_tile(1, j - 1), ks || j - 1 >= us.nt0, pv_cnt_b, o_use_b))
+                            break;
                         umma_commit_warp(&sh.v_empty[vt % NSV]);
                         if (j - 1 == us.nt1 - 1) umma_commit_warp(&sh.o_full[1]);  // O_B complete
                     }
@@ -539,7 +547,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                     if (j < us.nt0) {
                         const uint32_t vt = v_it + key_tile(0, j);
-                        if (!issue_pv(0, j, vt, pv_cnt_a, o_use_a)) break;
+                        if (!issue_pv(0, j, vt, (int)key_tile(0, j), true, pv_cnt_a, o_use_a)) break;
                         if (k_after_a) umma_commit_warp(&sh.v_empty[vt % NSV]);
                         if (j == us.nt0 - 1) umma_commit_warp(&sh.o_full[0]);  // O_A complete
                     }
@@ -547,7 +555,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (ok && us.nt1 > 0 && steps - 1 < us.nt1) {
                     // the last PV_B, after the loop
                     const uint32_t vt = v_it + key_tile(1, steps - 1);
-                    if (issue_pv(1, steps - 1, vt, pv_cnt_b, o_use_b)) {
+                    if (issue_pv(1, steps - 1, vt, (int)key_tile(1, steps - 1), ks || steps - 1 >= us.nt0, pv_cnt_b,
+                                 o_use_b)) {
                         umma_commit_warp(&sh.v_empty[vt % NSV]);
                         umma_commit_warp(&sh.o_full[1]);
                     }
@@ -714,7 +723,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t tS = lane_base + x * kKT;
         const uint32_t tO = lane_base + Cfg::kTmemO + x * D;
         const float sl = a.scale_log2;
-        uint32_t tcnt = 0;  // tiles of this query tile processed (s_full / pv_done phases)
+        uint32_t tcnt = 0;  // tiles of this pipeline processed (s_full phases)
         uint32_t ecnt = 0;  // units handed to the epilogue
         bool ok = true;
         for (int it = 0;; ++it) {
@@ -781,17 +790,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                         for (int k = 0; k < 128; ++k) s[k] = (k < lim) ? s[k] : -INFINITY;
                     }
-                    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                    // row maximum: eight independent max3 chains, then a tree
+                    float mx[8];
 #pragma unroll
-                    for (int k = 4; k < 124; k += 8) {
-                        mx0 = max3(mx0, s[k], s[k + 1]);
-                        mx1 = max3(mx1, s[k + 2], s[k + 3]);
-                        mx2 = max3(mx2, s[k + 4], s[k + 5]);
-                        mx3 = max3(mx3, s[k + 6], s[k + 7]);
+                    for (int c = 0; c < 8; ++c) mx[c] = s[c];
+#pragma unroll
+                    for (int k = 8; k < 120; k += 16) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[k + 2 * c], s[k + 2 * c + 1]);
                     }
-                    mx0 = max3(mx0, s[124], s[125]);
-                    mx1 = max3(mx1, s[126], s[127]);
-                    const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mx[c] = max3(mx[c], s[120 + 2 * c], s[121 + 2 * c]);
+                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                                       sl;
                     const bool move =
                         (tmax > m_ref + kRescaleThreshold2) || (m_ref == -INFINITY && tmax > -INFINITY);
                     float alpha = 1.f;
@@ -824,14 +836,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                     l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                     if (j >= 1 && __any_sync(0xffffffffu, move)) {
-                        // rescale O once PV_X(j - 1) has completed; PV_X(j)
-                        // cannot start before this warp's arrival below
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait_or_abort(&sh.pv_done[x], (tcnt - 1) & 1u, LIM, abort_flag))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                        // rescale O: PV_X(j - 1) has completed, as the commit
+                        // behind s_full (after S_X(j)) tracks every MMA the MMA
+                        // warp issued before it; PV_X(j) cannot start before
+                        // this warp's arrival below
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t r[32];
