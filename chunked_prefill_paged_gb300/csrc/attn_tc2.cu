@@ -87,15 +87,16 @@ struct Tc2Cfg {
     static constexpr int kHalves = D / 64;          // 64-element (128 B) column chunks
     static constexpr int kTileBytes = 128 * D * 2;  // 128 rows of D bf16 (a Q, K or V tile)
     static constexpr int kHalfBytes = kTileBytes / kHalves;
-    static constexpr int kKStages = (D == 128) ? 3 : 6;
+    static constexpr int kQSlots = 3;  // a unit's Q tiles take the next one or two
+    static constexpr int kKStages = (D == 128) ? 2 : 6;
     static constexpr int kVStages = (D == 128) ? 2 : 4;
     // Q_A, Q_B, the K ring, the V ring; the barriers and small arrays follow
-    static constexpr int kTileArea = kTileBytes * (2 + kKStages + kVStages);
+    static constexpr int kTileArea = kTileBytes * (kQSlots + kKStages + kVStages);
     static constexpr uint32_t kTmemO = 256;         // O_A; O_B at kTmemO + D
 };
 
 struct __align__(8) Tc2Shared {
-    uint64_t q_full[2], q_empty[2];  // per query tile
+    uint64_t q_full[3], q_empty[3];  // per Q slot
     uint64_t k_full[6], k_empty[6];
     uint64_t v_full[4], v_empty[4];
     uint64_t v_ready[4];             // a V tile may be read: landed, partial rows zeroed
@@ -158,8 +159,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (threadIdx.x == 0) record_error(a.err, kErrTimeout);
         return;
     }
-    uint8_t *sQ = smem_raw;        // Q_A, then Q_B
-    uint8_t *sK = smem_raw + 2 * TB;
+    uint8_t *sQ = smem_raw;  // Cfg::kQSlots Q slots
+    uint8_t *sK = smem_raw + Cfg::kQSlots * TB;
     uint8_t *sV = sK + NSK * TB;
     Tc2Shared &sh = *reinterpret_cast<Tc2Shared *>(smem_raw + Cfg::kTileArea);
 
@@ -171,9 +172,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int end_index = total_units + a.write_chunks;  // then the fused K/V write
 
     if (tid == 0) {
+        for (int q = 0; q < Cfg::kQSlots; ++q) {
+            mbar_init(&sh.q_full[q], 1);
+            mbar_init(&sh.q_empty[q], 1);
+        }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(&sh.q_full[x], 1);
-            mbar_init(&sh.q_empty[x], 1);
             mbar_init(&sh.s_full[x], 1);
             mbar_init(&sh.p_full[x], 4);  // the four softmax warps of the tile
             mbar_init(&sh.o_full[x], 1);
@@ -382,16 +385,28 @@ __global__ void __launch_bounds__(kThreads2, 1)
             __syncwarp();
         } else if (warp == kQWarp) {
             // ============================================================== Q
+            // A unit's query tiles go to the next one or two of three Q slots
+            // (tile A, then tile B of a row pair), so the next unit's tile A
+            // lands in the slot no running unit holds while this one runs.
             bool ok = true;
-            uint32_t fill_a = 0, fill_b = 0;  // Q_A / Q_B fills issued
-            // Q_X of the unit into its stage once the previous unit's S MMAs
-            // have released it
-            auto load_q = [&](int x, uint32_t fills) -> bool {
-                if (fills >= 1 &&
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[x], (fills - 1) & 1u, LIM, abort_flag)))
+            uint32_t qpos = 0;      // Q slots handed out
+            uint32_t filled = 0;    // bit q: slot q has been filled
+            uint32_t fill_par = 0;  // bit q: parity of slot q's fills
+            auto load_q = [&](int tok, int g) -> bool {
+                const int q = (int)(qpos % Cfg::kQSlots);
+                // the slot's previous tile must be done with: the commit after
+                // the last S MMA that read it
+                if (((filled >> q) & 1u) &&
+                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[q], ((fill_par >> q) & 1u) ^ 1u, LIM,
+                                                                abort_flag)))
                     return false;
-                if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[x], (uint32_t)TB);
+                if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[q], (uint32_t)TB);
                 __syncwarp();
+                if (lane < Cfg::kHalves)
+                    tma_load_3d(sQ + q * TB + lane * HB, &tm_q, &sh.q_full[q], lane * 64, g * a.G, tok);
+                filled |= 1u << q;
+                fill_par ^= 1u << q;
+                ++qpos;
                 return true;
             };
             for (int it = 0;; ++it) {
@@ -407,33 +422,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const int ntiles = u.rows > kTcTileM ? 2 : 1;
                 const int tok0 = u.cu0 + u.row0 / a.G;
                 const int tok_per_tile = kTcTileM / a.G;
-                // into L2 now; the copies below wait for the stages
+                // into L2 now; the copies below wait for their slots
                 if (lane < ntiles * Cfg::kHalves)
                     tma_prefetch_l2_3d(&tm_q, (lane % Cfg::kHalves) * 64, u.g * a.G,
                                        tok0 + (lane / Cfg::kHalves) * tok_per_tile);
-                if (!load_q(0, fill_a)) {
+                if (!load_q(tok0, u.g) || (ntiles == 2 && !load_q(tok0 + tok_per_tile, u.g))) {
                     ok = false;
                     break;
-                }
-                if (lane < Cfg::kHalves) tma_load_3d(sQ + lane * HB, &tm_q, &sh.q_full[0], lane * 64, u.g * a.G, tok0);
-                ++fill_a;
-                if (ntiles == 2) {
-                    if (!load_q(1, fill_b)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane < Cfg::kHalves)
-                        tma_load_3d(sQ + TB + lane * HB, &tm_q, &sh.q_full[1], lane * 64, u.g * a.G,
-                                    tok0 + tok_per_tile);
-                    ++fill_b;
                 }
             }
             if (!ok) {
                 if (lane == 0) record_error(a.err, kErrTimeout);
                 *abort_flag = 1;
             }
-            if (fill_a >= 1) mbar_wait(&sh.q_full[0], (fill_a - 1) & 1u, LIM);
-            if (fill_b >= 1) mbar_wait(&sh.q_full[1], (fill_b - 1) & 1u, LIM);
+            // drain: every slot's last copy must land before the CTA may exit
+            for (int q = 0; q < Cfg::kQSlots; ++q)
+                if ((filled >> q) & 1u) mbar_wait(&sh.q_full[q], ((fill_par >> q) & 1u) ^ 1u, LIM);
             __syncwarp();
         } else if (warp == kMmaWarp2) {
             // ============================================================ MMA
@@ -442,11 +446,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             const uint64_t q_desc = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
             const uint32_t desc_hi = (uint32_t)(q_desc >> 32);
-            const uint32_t qa_lo = (uint32_t)q_desc, qb_lo = (uint32_t)q_desc + (uint32_t)(TB >> 4);
+            const uint32_t q_lo0 = (uint32_t)q_desc;
             const uint32_t k_lo0 = (uint32_t)smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
             const uint32_t v_lo0 = (uint32_t)smem_desc(smem_u32(sV), HB, 1024, kSwizzle128B);
             uint32_t k_it = 0, v_it = 0;     // K / V tiles consumed (ring position)
-            uint32_t q_use_a = 0, q_use_b = 0;    // units that used Q_X
+            uint32_t qpos = 0;     // Q slots taken (as the Q warp hands them out)
+            uint32_t q_par = 0;    // bit q: parity of the uses of Q slot q
             uint32_t pv_cnt_a = 0, pv_cnt_b = 0;  // PV_X issued (p_full parity)
             uint32_t o_use_a = 0, o_use_b = 0;    // units that accumulated into O_X
             auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -510,6 +515,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 // S_X(j) and PV_X(j) read key tile key_tile(x, j) of the unit
                 auto key_tile = [&](int x, int j) -> uint32_t { return (uint32_t)(ks ? 2 * j + x : j); };
                 const int steps = ks ? us.nt0 : n;
+                // Q slots of tile A and (row pair) tile B, as the Q warp filled them
+                const int qa = (int)(qpos % Cfg::kQSlots), qb = (int)((qpos + 1) % Cfg::kQSlots);
+                const uint32_t qa_lo = q_lo0 + (uint32_t)qa * (uint32_t)(TB >> 4);
+                const uint32_t qb_lo = q_lo0 + (uint32_t)qb * (uint32_t)(TB >> 4);
                 // K(kt) is freed after its last S: S_B in row pairs, the one S otherwise
                 const bool k_after_a = ks || us.nt1 == 0;
                 for (int j = 0; j < steps && ok; ++j) {
@@ -517,12 +526,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         const uint32_t kt = k_it + key_tile(0, j);
                         const int ks_ = (int)(kt % NSK);
                         if (!wait(&sh.k_full[ks_], (kt / NSK) & 1u)) break;
-                        if (j == 0 && !wait(&sh.q_full[0], q_use_a & 1u)) break;
+                        if (j == 0 && !wait(&sh.q_full[qa], (q_par >> qa) & 1u)) break;
                         tc_fence_after();
                         issue_s(0, qa_lo, k_lo0 + (uint32_t)ks_ * (uint32_t)(TB >> 4));
                         if (k_after_a) umma_commit_warp(&sh.k_empty[ks_]);
                         // Q_A is free after the last S that reads it
-                        if ((int)key_tile(0, j) == (ks ? n - 1 : us.nt0 - 1)) umma_commit_warp(&sh.q_empty[0]);
+                        if ((int)key_tile(0, j) == (ks ? n - 1 : us.nt0 - 1)) umma_commit_warp(&sh.q_empty[qa]);
                     }
                     // PV_B(j - 1): tile B is the last reader of its V tile
                     if (j >= 1 && j - 1 < us.nt1) {
@@ -538,12 +547,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         // a key-split unit's own K tile; in a row pair, K(j) when
                         // tile A's keys ended before it
                         if ((ks || j >= us.nt0) && !wait(&sh.k_full[ks_], (kt / NSK) & 1u)) break;
-                        if (!ks && j == 0 && !wait(&sh.q_full[1], q_use_b & 1u)) break;
+                        if (!ks && j == 0 && !wait(&sh.q_full[qb], (q_par >> qb) & 1u)) break;
                         tc_fence_after();
                         issue_s(1, ks ? qa_lo : qb_lo, k_lo0 + (uint32_t)ks_ * (uint32_t)(TB >> 4));
                         umma_commit_warp(&sh.k_empty[ks_]);
                         if (ks ? (int)key_tile(1, j) == n - 1 : j == us.nt1 - 1)
-                            umma_commit_warp(&sh.q_empty[ks ? 0 : 1]);
+                            umma_commit_warp(&sh.q_empty[ks ? qa : qb]);
                     }
                     if (j < us.nt0) {
                         const uint32_t vt = v_it + key_tile(0, j);
@@ -562,8 +571,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                 }
                 if (!ok) break;
-                ++q_use_a;
-                if (!ks) ++q_use_b;
+                q_par ^= 1u << qa;
+                if (!ks) q_par ^= 1u << qb;
+                qpos += ks ? 1 : 2;
                 ++o_use_a;
                 if (us.nt1 > 0) ++o_use_b;
                 k_it += (uint32_t)n;
