@@ -586,10 +586,14 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     tc_fence_after();
                     const uint32_t k_lo = k_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
                     const uint32_t d_tmem = tmem + ub * kKT;
+                    if constexpr (D == 128) {
+                        umma_s_tile128(d_tmem, q_lo_u, k_lo, desc_hi, idesc_s, (uint32_t)(HB >> 4));
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
-                        umma_ss_warp2(d_tmem, q_lo_u + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
+                            umma_ss_warp2(d_tmem, q_lo_u + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                        }
                     }
                     umma_commit_warp(&sh.s_full[ub]);
                     umma_commit_warp(&sh.k_empty[rs]);
@@ -643,10 +647,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     tc_fence_after();
                     const uint32_t v_lo = v_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
                     const uint32_t tP = tmem + ub * kKT;
-#pragma unroll
-                    for (int kk = 0; kk < kKT / 16; ++kk)
-                        umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
-                                      (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_pv_tile128(tO, tP, v_lo, desc_hi, idesc_pv, j > 0 ? 1u : 0u);
                     umma_commit_warp(&sh.v_empty[rs]);
                     umma_commit_warp(&sh.pv_done[ub]);
                     if (j == n - 1) umma_commit_warp(&sh.o_full);

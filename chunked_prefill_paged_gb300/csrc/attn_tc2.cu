@@ -75,11 +75,11 @@ constexpr int kReaders2 = 15;          // every warp but 8 reads every unit
 constexpr float kRescaleThreshold2 = 8.0f;  // log2 units
 // Registers per thread: the launch gives 128 to each of the 512 threads; the
 // two softmax warpgroups take 184 (a row's 128 scores stay in registers),
-// warps 8-11 keep 88 and the epilogue warpgroup 56 (2 x 184 + 88 + 56 =
+// warps 8-11 keep 80 and the epilogue warpgroup 64 (2 x 184 + 80 + 64 =
 // 4 x 128; a split that compiles without spills).
 constexpr uint32_t kRegsSoftmax = 184;
-constexpr uint32_t kRegsOther = 88;
-constexpr uint32_t kRegsEpilogue = 56;
+constexpr uint32_t kRegsOther = 80;
+constexpr uint32_t kRegsEpilogue = 64;
 constexpr int kLaunchRegs = 128;
 
 template <int D>
@@ -462,10 +462,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
             // S_X(j) = Q K(kt)^T into S_X (Q: the unit's tile X, or tile A for
             // both pipelines of a key-split unit), then its commit
             auto issue_s = [&](int x, uint32_t qd, uint32_t k_lo) {
+                if constexpr (D == 128) {
+                    umma_s_tile128(tmem + x * kKT, qd, k_lo, desc_hi, idesc_s, (uint32_t)(HB >> 4));
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
-                    umma_ss_warp2(tmem + x * kKT, qd + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(((kk >> 2) * HB + (kk & 3) * 32) >> 4);
+                        umma_ss_warp2(tmem + x * kKT, qd + off, k_lo + off, desc_hi, idesc_s, kk > 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit_warp(&sh.s_full[x]);
             };
@@ -489,10 +493,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint32_t v_lo = v_lo0 + (uint32_t)vs * (uint32_t)(TB >> 4);
                 const uint32_t tP = tmem + x * kKT;
                 const uint32_t tO = tmem + Cfg::kTmemO + x * D;
-#pragma unroll
-                for (int kk = 0; kk < kKT / 16; ++kk)
-                    umma_ts_warp2(tO, tP + kk * 8, v_lo + (uint32_t)((kk * 2048) >> 4), desc_hi, idesc_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                umma_pv_tile128(tO, tP, v_lo, desc_hi, idesc_pv, j > 0 ? 1u : 0u);
                 ++pv_cnt;
                 return true;
             };

@@ -251,6 +251,69 @@ __device__ __forceinline__ void umma_ts_warp2(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// One score tile S = Q K^T at head_dim 128: eight MMAs (K steps of 16
+// elements) issued by one elected lane under a single elect.sync.  Q and K
+// are K-major 128-byte-swizzled tiles of two 64-column halves; a K step
+// advances both descriptors' start address by 32 bytes (2 in 16-byte units)
+// and the second half starts half_units later.  The first MMA overwrites D.
+__device__ __forceinline__ void umma_s_tile128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
+                                               uint32_t idesc, uint32_t half_units) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 a, b;\n\t.reg .b64 ad, bd;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "mov.b64 ad, {%1, %3};\n\tmov.b64 bd, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pf;\n\t"
+        "add.u32 a, %1, 2;\n\tadd.u32 b, %2, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, 4;\n\tadd.u32 b, %2, 4;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, 6;\n\tadd.u32 b, %2, 6;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, %5;\n\tadd.u32 b, %2, %5;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, b, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, b, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, b, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, pt;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(half_units)
+        : "memory");
+}
+
+// One PV product over a 128-key tile: O (+)= P V with P read from TMEM
+// (16 keys = 8 columns of bf16 pairs per MMA) and V an MN-major tile (16 key
+// rows = 2048 bytes = 128 units per MMA); eight MMAs under one elect.sync.
+// The first MMA accumulates only when accumulate is non-zero.
+__device__ __forceinline__ void umma_pv_tile128(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_lo, uint32_t desc_hi,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 t, b;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "mov.b64 bd, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p0;\n\t"
+        "add.u32 t, %1, 8;\n\tadd.u32 b, %2, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t"
+        "add.u32 t, t, 8;\n\tadd.u32 b, b, 128;\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], bd, %4, pt;\n\t}\n" ::"r"(d_tmem),
+        "r"(p_tmem), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit_warp(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
