@@ -25,6 +25,12 @@
 //              the work counter, so CTAs whose attention work has run out take
 //              them (this kernel reads new keys from k_new / v_new, so the
 //              pool rows are only needed by the next call).
+//              With the rotary embedding they first rotate the launch's new
+//              keys, once, from k_src into the workspace copy k_new that the
+//              new-key tiles and the fused write read: pieces of 16 tokens
+//              taken from their own counter, each counted done per 128-row
+//              tile of the new rows, which the K copies of a new-key tile
+//              wait for.
 //   warp 8     unit scheduler (it claims each unit, decodes it once and passes
 //              the decoded unit to the other roles through a ring) and TMA
 //              producer of Q per unit and of the K tiles; warp 10 of the V
@@ -38,7 +44,11 @@
 //   warp 11    PV MMA issuer: O += P(j) V(j) once the softmax has written P(j).
 //              Issuing from two warps on different SM sub-partitions halves
 //              the instruction stream each shares with the softmax warps.
-//   warps 12-15 (FP8 pools only) expand E4M3 code tiles in place into the
+//   warps 12-15 (BF16 pools) output epilogue; with the rotary embedding they
+//              also rotate each unit's query tile in its Q stage once it has
+//              landed, one unit ahead of the outputs, and the score MMAs wait
+//              for that (q_rot) instead of the copy.
+//   warps 12-15 (FP8 pools) expand E4M3 code tiles in place into the
 //              fp16 tiles the MMAs read (K: 12-13, V: 14-15).
 //
 // TMEM (512 columns): three score buffers S0 [0,128), S1 [128,256) and
@@ -58,6 +68,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -78,6 +89,14 @@ constexpr int kPvWarp = 11;           // PV MMA issuer
 constexpr int kSBuf = 3;              // score buffers in TMEM
 constexpr uint32_t kTmemO = kSBuf * kKT;  // first TMEM column of O
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// BF16 pools: during a direct unit of at least kEarlyClaimMinTiles key tiles,
+// and during every unit with the rotary embedding, the next unit is claimed
+// after issuing the K copies of all but the last kClaimAhead + 1 tiles
+// (measured on the 10k-token Llama prompt: the last chunk 0.194 -> 0.189 ms,
+// with RoPE 0.200 -> 0.194 ms; shorter units, decode pieces among them, keep
+// the late claim, which balances the launch's last wave better)
+constexpr int kClaimAhead = 6;
+constexpr int kEarlyClaimMinTiles = 24;
 constexpr int kKConvWarp = 12;              // FP8 cache: warps 12-13 expand K tiles, 14-15 V tiles
 constexpr int kEpiWarp = 12;                // BF16 cache: warps 12-15 write the outputs
 
@@ -113,6 +132,7 @@ struct TcCfg {
 
 struct __align__(8) TcShared {
     uint64_t q_full[2], q_empty[2];
+    uint64_t q_rot[2];  // rotary embedding: the stage's queries are rotated (four epilogue warps)
     uint64_t k_full[6], k_empty[6];
     uint64_t v_full[6], v_empty[6];
     uint64_t s_full[kSBuf];  // per score buffer
@@ -130,6 +150,7 @@ struct __align__(8) TcShared {
     UnitRing ring;
     uint32_t tmem_base;
     int abort_flag;
+    int rope_claim;  // the softmax warps' current piece of the key rotation
 };
 
 // Four E4M3 codes (bytes of w, lowest address first) as fp16 pairs: codes
@@ -273,6 +294,165 @@ __device__ __forceinline__ void merge_tail_rows(const AttnArgs &a, const Unit &u
     }
 }
 
+// Piece `piece` of the key rotation: new tokens [16 piece, 16 piece + 16) of
+// every kv head, from k_src into k_new, by the 256 softmax threads.  Thread
+// (tl, j, s) takes the pairs (c, c + D/2), c = 8 j .. 8 j + 7, of token tl's
+// rows for kv heads s, s + S, ... (S threads per (token, j)): two 16-byte
+// loads per row, every load of the piece in flight before the first store.
+template <int D>
+__device__ __forceinline__ void rope_keys_piece(const AttnArgs &a, int piece, int tid) {
+    constexpr int J = D / 16;                            // 8-pair chunks of a row
+    constexpr int S = kSoftmaxThreads / (kRopePieceTokens * J);  // threads per (token, chunk)
+    constexpr int HB = 4;                                // heads per batch of loads
+    static_assert(S >= 1 && S * kRopePieceTokens * J == kSoftmaxThreads, "one (token, chunk, s) per thread");
+    const int s = tid % S, combo = tid / S;
+    const int tl = combo / J, j = combo - tl * J;
+    const int t = piece * kRopePieceTokens + tl;
+    if (t >= a.total_tokens) return;
+    const long long row0 = (long long)t * a.hkv * D + 8 * j;
+    const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.k_src) + row0;
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.k_new)) + row0;
+    float cs[8], sn[8];
+    for (int h0 = s; h0 < a.hkv; h0 += HB * S) {
+        uint4 x[HB], y[HB];
+#pragma unroll
+        for (int i = 0; i < HB; ++i) {
+            const int h = h0 + i * S;
+            if (h < a.hkv) {
+                x[i] = __ldg(reinterpret_cast<const uint4 *>(src + h * D));
+                y[i] = __ldg(reinterpret_cast<const uint4 *>(src + h * D + D / 2));
+            }
+        }
+        if (h0 == s) {
+            // the position and the angles while the first rows load
+            const int r = request_of_token(a.cu, a.num_reqs, t);
+            const int pos = __ldg(a.cached + r) + (t - __ldg(a.cu + r));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) rope_cos_sin(pos, a.turn_frac[8 * j + k], cs[k], sn[k]);
+        }
+#pragma unroll
+        for (int i = 0; i < HB; ++i) {
+            const int h = h0 + i * S;
+            if (h >= a.hkv) break;
+            const uint32_t xw[4] = {x[i].x, x[i].y, x[i].z, x[i].w}, yw[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+            uint32_t ow[4], pw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // element 2k in the low half of word k
+                float a0, b0, a1, b1;
+                rope_turn(__uint_as_float(xw[k] << 16), __uint_as_float(yw[k] << 16), cs[2 * k], sn[2 * k], a0, b0);
+                rope_turn(__uint_as_float(xw[k] & 0xffff0000u), __uint_as_float(yw[k] & 0xffff0000u), cs[2 * k + 1],
+                          sn[2 * k + 1], a1, b1);
+                ow[k] = pack_bf16(a0, a1);
+                pw[k] = pack_bf16(b0, b1);
+            }
+            *reinterpret_cast<uint4 *>(dst + h * D) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            *reinterpret_cast<uint4 *>(dst + h * D + D / 2) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        }
+    }
+}
+
+// Whether the key rotation's pieces of the new rows [row_begin, row_end) are
+// done: waits (bounded)
+// for the pieces of their 128-row tiles, or of the whole launch once `all`
+// is known.  The calling thread's acquire orders its later reads after them.
+__device__ __forceinline__ bool rope_rows_done(const AttnArgs &a, int row_begin, int row_end, bool &all,
+                                               long long limit, const volatile int *abort_flag) {
+    if (!all) {
+        const long long t0 = clock64();
+        for (;;) {
+            if (ld_acquire_gpu(a.rope_count + 1) >= a.rope_pieces) {
+                all = true;
+                break;
+            }
+            bool have = true;
+            for (int i = row_begin / kTcTileN; i <= (row_end - 1) / kTcTileN && have; ++i)
+                have = ld_acquire_gpu(a.rope_count + 2 + i) >= rope_pieces_of_tile(a.total_tokens, i);
+            if (have) break;
+            if (*abort_flag || clock64() - t0 > limit) return false;
+            __nanosleep(128);
+        }
+    }
+    return true;
+}
+
+// As rope_rows_done, for the lane that then issues copies of the rotated
+// rows: its proxy fence orders them before its TMA reads too.
+__device__ __forceinline__ bool rope_rows_ready(const AttnArgs &a, int row_begin, int row_end, bool &all,
+                                                long long limit, const volatile int *abort_flag) {
+    if (!rope_rows_done(a, row_begin, row_end, all, limit, abort_flag)) return false;
+    fence_proxy_async_global();
+    return true;
+}
+
+// Rotate the queries of unit u in place in its Q stage (128 rows of D bf16
+// values, in 64-column halves of 128-byte swizzled rows), by the 128
+// epilogue threads (thread lr).  Item (tl, fc): the pairs (c, c + D/2), c =
+// 8 fc .. 8 fc + 7, of the G rows of the tile's local token tl, all at
+// position C + row0 / G + tl; thread lr takes items lr, lr + 128, ..., so
+// its fc = lr mod D/16 is fixed, and it reads those pairs' turn rates once
+// per tile.  The top 32 bits of pos * rate modulo 2^64 (the high word's
+// product plus the carry-in from the low word's: exact to 2^-32 turn) give
+// the angle, whose top 24 bits go to sincospif as for the keys, so the
+// rotated queries round as an exact rotation's do but for rare ties.
+// Elements c and c + D/2 sit in 16-byte chunks at the same place of their
+// halves (D = 128) or four chunks apart in one half (D = 64).
+template <int D>
+__device__ __forceinline__ void rope_q_tile(const AttnArgs &a, const Unit &u, uint8_t *tile, int lr) {
+    constexpr int FC = D / 16;
+    constexpr int HB = 128 * 128;  // bytes of a 64-column half
+    const int G = a.G;
+    const int items = cdiv(u.rows, G) * FC;
+    const int fc = lr % FC;
+    uint32_t fh[8], fl[8];  // the pairs' turn rates, high and low words
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const unsigned long long f = a.turn_frac[fc * 8 + k];
+        fh[k] = (uint32_t)(f >> 32);
+        fl[k] = (uint32_t)f;
+    }
+    const int e0 = fc * 8, e1 = e0 + D / 2;
+    const int off0 = (e0 >> 6) * HB, c0 = (e0 & 63) >> 3;
+    const int off1 = (e1 >> 6) * HB, c1 = (e1 & 63) >> 3;
+    for (int it = lr; it < items; it += 128) {
+        const int tl = it / FC;
+        const uint32_t pos = (uint32_t)(u.C + u.row0 / G + tl);
+        float2 c2[4], s2[4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // the angle's top 24 bits (units of 2^-24 turn) as an exact float
+            // x in [0, 2) half turns
+            const uint32_t v = (pos * fh[k] + __umulhi(pos, fl[k])) >> 8;
+            const float x = __uint2float_rn(v) * (1.0f / 8388608.0f);
+            float sv, cv;
+            sincospif(x, &sv, &cv);
+            (k & 1 ? c2[k >> 1].y : c2[k >> 1].x) = cv;
+            (k & 1 ? s2[k >> 1].y : s2[k >> 1].x) = sv;
+        }
+#pragma unroll 2
+        for (int g = 0; g < G; ++g) {
+            const int m = tl * G + g;
+            uint4 *p0 = reinterpret_cast<uint4 *>(tile + off0 + m * 128 + ((c0 ^ (m & 7)) << 4));
+            uint4 *p1 = reinterpret_cast<uint4 *>(tile + off1 + m * 128 + ((c1 ^ (m & 7)) << 4));
+            const uint4 x = *p0, y = *p1;
+            const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+            uint32_t ow[4], pw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // elements 2k (low half of word k) and 2k + 1: (x c - y s, y c + x s)
+                const float2 xf = make_float2(__uint_as_float(xw[k] << 16), __uint_as_float(xw[k] & 0xffff0000u));
+                const float2 yf = make_float2(__uint_as_float(yw[k] << 16), __uint_as_float(yw[k] & 0xffff0000u));
+                const float2 o = __ffma2_rn(xf, c2[k], __fmul2_rn(yf, make_float2(-s2[k].x, -s2[k].y)));
+                const float2 q = __ffma2_rn(yf, c2[k], __fmul2_rn(xf, s2[k]));
+                ow[k] = pack_bf16(o.x, o.y);
+                pw[k] = pack_bf16(q.x, q.y);
+            }
+            *p0 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            *p1 = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        }
+    }
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -302,6 +482,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     if (tid == 0) {
         for (int b = 0; b < Cfg::kQStages; ++b) {
             mbar_init(&sh.q_full[b], 1);
+            mbar_init(&sh.q_rot[b], 4);
             // the last score MMA's commit, and with BF16 pools the four
             // epilogue warps, which stage the unit's output rows there
             mbar_init(&sh.q_empty[b], TcRoles<F8>::kEpiWarps ? 1 + 4 : 1);
@@ -366,29 +547,44 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
         int pending = 0;      // fills of the ring issued and not yet drained (<= ns)
+        bool rope_all = false;  // rotary embedding: every rotated key row is known written (lane 0)
         // Warp 8 is also the scheduler: lane 0 takes the next unit from the
         // work counter once it has issued the current unit's last K copies,
-        // a few tiles before the CTA runs out of work (claimed any earlier,
+        // a few tiles before the CTA runs out of work (claimed much earlier,
         // the last units would wait behind busy CTAs while others idle), and
         // publishes it to the other roles through the unit ring.
+        //
+        // Long direct units (BF16 pools), and with the rotary embedding every
+        // unit, claim the next unit kClaimAhead tiles earlier and publish it a
+        // tile after that, with its Q copy issued then if its stage is free:
+        // the next unit's first score MMA need not wait for its queries (nor,
+        // with the rotary embedding, for their rotation by the epilogue warps).
         int taken = (kv_role == 0 && lane == 0) ? atomicAdd(a.sched, 1) : 0;
+        int early = -1;        // ring entry published during the previous unit (rotary embedding)
+        bool early_q = false;  // and its Q copy issued
         for (int it = 0;; ++it) {  // it: units started by this CTA
             int unit;
             Unit u;
             if (kv_role == 0) {
-                unit = __shfl_sync(0xffffffffu, taken, 0);
-                const int s = it % kUnitRing;
-                if (it >= kUnitRing &&
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.ring.empty[s],
-                                                                (uint32_t)((it / kUnitRing - 1) & 1), LIM, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                if (unit < total_units) decode_unit(a, unit, u);  // once, for every role
-                if (lane == 0) {
-                    publish_unit(sh.ring, it, unit, u);
-                    // pieces of the K/V write need no copies: claim the next index now
-                    if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
+                if (early == it) {
+                    unit = *reinterpret_cast<volatile int *>(&sh.ring.index[it % kUnitRing]);
+                    if (unit < total_units) get_unit(u, sh.ring.desc[it % kUnitRing]);
+                } else {
+                    unit = __shfl_sync(0xffffffffu, taken, 0);
+                    const int s = it % kUnitRing;
+                    if (it >= kUnitRing &&
+                        !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.ring.empty[s], (uint32_t)((it / kUnitRing - 1) & 1),
+                                                                    LIM, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (unit < total_units) decode_unit(a, unit, u);  // once, for every role
+                    if (lane == 0) {
+                        publish_unit(sh.ring, it, unit, u);
+                        // pieces of the K/V write need no copies: claim the next index now
+                        if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
+                    }
+                    __syncwarp();
                 }
             } else {
                 unit = read_unit(sh.ring, it, LIM, abort_flag, u);
@@ -469,6 +665,19 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                             tma_load_4d(dst + h * HB + b * a.bs * 128, kv ? &tm_v_pool : &tm_k_pool, full, h * 64,
                                         u.g, 0, blk);
                     }
+                } else if (!F8 && a.rope && kv == 0) {
+                    // rotated keys: lane 0 waits until the rows are written,
+                    // then issues the copies itself
+                    const int row = u.cu0 + (key0 - u.C);
+                    int ready = 1;
+                    if (lane == 0) ready = rope_rows_ready(a, row, row + valid, rope_all, LIM, abort_flag) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, (uint32_t)TB);
+#pragma unroll
+                        for (int h = 0; h < Cfg::kHalves; ++h)
+                            tma_load_3d(dst + h * HB, &tm_k_new, full, h * 64, u.g, row);
+                    }
                 } else {
                     if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)TB);
                     __syncwarp();
@@ -488,20 +697,66 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 // ago and is free by now, while the first K tile waits for a
                 // ring slot that the current unit's last score MMAs release
                 constexpr int QS = Cfg::kQStages;
-                const int qb = it % QS;
-                if (ok && it >= QS &&
-                    !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_empty[qb], (uint32_t)(((it - QS) / QS) & 1), LIM,
-                                                                abort_flag)))
-                    ok = false;
-                if (ok) {
+                // the Q copy of ring entry i (unit fields uq) into stage i % QS
+                // once its previous user released it (wait), or only if it
+                // already has (!wait)
+                auto copy_q = [&](int i, const Unit &uq, bool wait) -> bool {
+                    const int qb = i % QS;
+                    if (i >= QS) {
+                        const uint32_t par = (uint32_t)(((i - QS) / QS) & 1);
+                        if (!__all_sync(0xffffffffu, wait ? mbar_wait_or_abort(&sh.q_empty[qb], par, LIM, abort_flag)
+                                                          : mbar_try_wait(&sh.q_empty[qb], par)))
+                            return false;
+                    }
                     if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qb], TB);
                     __syncwarp();
-                    const int tok0 = u.cu0 + u.row0 / a.G;
                     if (lane < Cfg::kHalves)
-                        tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, u.g * a.G, tok0);
+                        tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, uq.g * a.G,
+                                    uq.cu0 + uq.row0 / a.G);
+                    return true;
+                };
+                if (ok && !(early == it && early_q) && !copy_q(it, u, true)) ok = false;
+                const int jc = (!F8 && (a.rope || (u.piece < 0 && n >= kEarlyClaimMinTiles))) ? max(0, n - 1 - kClaimAhead) : n;
+                early_q = false;
+                for (int j = 0; j < n && ok; ++j) {
+                    ok = load_kv(j, 0);
+                    if (!ok || j < jc) continue;
+                    if (j == jc) {
+                        if (lane == 0) taken = atomicAdd(a.sched, 1);
+                        continue;
+                    }
+                    if (early != it + 1) {
+                        // publish the next unit (its claim has had a tile to return)
+                        const int un = __shfl_sync(0xffffffffu, taken, 0);
+                        const int s = (it + 1) % kUnitRing;
+                        if (it + 1 >= kUnitRing &&
+                            !__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.ring.empty[s],
+                                                                        (uint32_t)(((it + 1) / kUnitRing - 1) & 1), LIM,
+                                                                        abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        Unit uu;
+                        if (un < total_units) decode_unit(a, un, uu);
+                        if (lane == 0) {
+                            publish_unit(sh.ring, it + 1, un, uu);
+                            if (un >= total_units && un < end_index) taken = atomicAdd(a.sched, 1);
+                        }
+                        __syncwarp();
+                        early = it + 1;
+                    }
+                    if (!early_q) {
+                        const int un = *reinterpret_cast<volatile int *>(&sh.ring.index[(it + 1) % kUnitRing]);
+                        if (un < total_units) {
+                            Unit uu;
+                            get_unit(uu, sh.ring.desc[(it + 1) % kUnitRing]);
+                            early_q = copy_q(it + 1, uu, false);
+                        }
+                    }
                 }
-                for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 0);
-                if (lane == 0) taken = atomicAdd(a.sched, 1);  // this unit's copies are all issued
+                // this unit's copies are all issued: claim the next unit now
+                // unless that was done above
+                if (ok && jc >= n && lane == 0) taken = atomicAdd(a.sched, 1);
             } else {
                 for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 1);
             }
@@ -565,9 +820,11 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             const int n = tl.n_total;
             if (s_role) {
                 // S(j) = Q K(j)^T, as far ahead as the score buffers allow
+                // (with the rotary embedding, once the epilogue warps rotated Q)
                 const int qb = ucnt % Cfg::kQStages;
+                uint64_t *q_ready = (!F8 && a.rope) ? &sh.q_rot[qb] : &sh.q_full[qb];
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&sh.q_full[qb], (uint32_t)((ucnt / Cfg::kQStages) & 1), LIM, abort_flag))) {
+                                mbar_wait_or_abort(q_ready, (uint32_t)((ucnt / Cfg::kQStages) & 1), LIM, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -678,19 +935,50 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // sums from the softmax warps, wait for the last PV, read O, free it
         // for the next unit's PVs, and write the rows (a split unit's or tail
         // piece's partial: unnormalised, with its maxima and sums).
+        //
+        // With the rotary embedding these warps rotate each unit's queries in
+        // its Q stage, one unit ahead: the next unit's as soon as its copy
+        // has landed, before this unit's outputs (which wait for its last PV).
         const int e = warp - kEpiWarp;
         const int lr = 32 * e + lane;
         const uint32_t tO = tmem + ((uint32_t)(32 * e) << 16) + kTmemO;
         bool ok = true;
+        const bool rope = !F8 && a.rope;
+        // the queries of ring entry i (an attention unit uq), rotated in place
+        auto rotate_q = [&](int i, const Unit &uq) -> bool {
+            const int qb = i % Cfg::kQStages;
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.q_full[qb], (uint32_t)((i / Cfg::kQStages) & 1), LIM,
+                                                            abort_flag)))
+                return false;
+            rope_q_tile<D>(a, uq, sQ + qb * TB, lr);
+            fence_proxy_async_smem();  // the score MMAs read Q through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_rot[qb]);
+            return true;
+        };
+        // (each entry's ring slot is held from its first read until its
+        // fields are read again, after the next unit's rotation: so the
+        // fields are not kept in registers meanwhile)
+        Unit u;
+        int unit = read_unit(sh.ring, 0, LIM, abort_flag, u, false);
+        if (rope && unit >= 0 && unit < total_units && !rotate_q(0, u)) unit = -1;
         for (int ec = 0;; ++ec) {
-            Unit u;
-            const int unit = read_unit(sh.ring, ec, LIM, abort_flag, u);
             if (unit < 0) {
                 ok = false;
                 break;
             }
             if (unit >= end_index) break;
-            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
+            int unit_n = 0;
+            if (rope) {
+                Unit un;
+                unit_n = read_unit(sh.ring, ec + 1, LIM, abort_flag, un, false);
+                if (unit_n >= 0 && unit_n < total_units && !rotate_q(ec + 1, un)) unit_n = -1;
+            }
+            reread_unit(sh.ring, ec, u);
+            if (unit >= total_units) {  // a piece of the K/V write: the softmax warps' job
+                unit = rope ? unit_n : read_unit(sh.ring, ec + 1, LIM, abort_flag, u, false);
+                continue;
+            }
             const uint32_t ph = (uint32_t)(ec & 1);
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.epi_full, ph, LIM, abort_flag))) {
                 ok = false;
@@ -805,6 +1093,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     merge_tail_rows<D>(a, u, 32 * e + 16, lane);
                 }
             }
+            unit = rope ? unit_n : read_unit(sh.ring, ec + 1, LIM, abort_flag, u, false);
         }
         if (!ok) {
             if (lane == 0) record_error(a.err, kErrTimeout);
@@ -873,6 +1162,28 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         int prev_b = 0;      // buffer and use parity of the previous tile (for the PV(j-1) wait)
         uint32_t prev_ph = 0;
         bool ok = true;
+        if (!F8 && a.rope) {
+            // the rotary embedding: rotate the new keys once, before any unit.
+            // Thread 0 claims the pieces for the eight warps, each one piece
+            // ahead; once every thread's rows are out (the barrier), it counts
+            // the piece done (release) for its 128-row tile and the launch.
+            int next = 0;
+            if (tid == 0) next = atomicAdd(a.rope_count, 1);
+            for (;;) {
+                if (tid == 0) sh.rope_claim = next;
+                named_bar_sync(1, kSoftmaxThreads);
+                const int piece = sh.rope_claim;
+                if (piece >= a.rope_pieces) break;
+                if (tid == 0) next = atomicAdd(a.rope_count, 1);
+                rope_keys_piece<D>(a, piece, tid);
+                fence_proxy_async_global();
+                named_bar_sync(1, kSoftmaxThreads);  // also: every thread has read rope_claim
+                if (tid == 0) {
+                    red_release_gpu_add(a.rope_count + 2 + piece / (kTcTileN / kRopePieceTokens), 1);
+                    red_release_gpu_add(a.rope_count + 1, 1);
+                }
+            }
+        }
         for (int oc = 0;; ++oc) {  // oc: units started
             Unit u;
             const int unit = read_unit(sh.ring, oc, LIM, abort_flag, u);
@@ -885,11 +1196,18 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 // a piece of the fused K/V write.  This kernel reads new keys
                 // from k_new / v_new, so the pool rows are only for the next
                 // call; CTAs take these pieces once attention work runs out.
+                // Rotated keys are read once the whole rotation is done.
+                bool rope_all = false;
+                if (!F8 && a.rope && !rope_rows_ready(a, 0, a.total_tokens, rope_all, LIM, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 const long long total = (long long)a.total_tokens * a.hkv * (D * 2 / 16);
                 const long long b = (long long)(unit - total_units) * kWriteChunkPieces;
                 const long long e = b + kWriteChunkPieces < total ? b + kWriteChunkPieces : total;
                 scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, D * 2,
-                               a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, kSoftmaxThreads, a.err);
+                               a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, kSoftmaxThreads, a.err,
+                               !F8 && a.rope);
                 continue;
             }
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;

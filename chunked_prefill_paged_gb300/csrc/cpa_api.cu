@@ -126,6 +126,7 @@ bool use_tensor_cores(const cpa_params *p) {
 struct Plan {
     int tile_m = 0;
     bool tc2 = false;        // the two-pipeline tensor-core kernel (attn_tc2.cu)
+    bool rope_fused = false; // the one-pipeline kernel rotates queries and keys itself
     int tiles_per_unit = 1;
     int head_major = 0;
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
@@ -296,6 +297,16 @@ int choose_tiles_per_unit(const cpa_batch *b, const cpa_params *p, int sms, cons
     return end_time(1) < 0.97 * end_time(2) ? 1 : 2;
 }
 
+// Ints at the workspace's counter offset, zeroed before each tensor-core
+// launch: the work counter, kSoftmaxWarpsMax per tail unit, and with the
+// rotary embedding the rotation's claim and done counts and one done count
+// per 128-row tile of the new rows.
+size_t counter_ints(const cpa_batch *b, const Plan &pl) {
+    size_t n = 1 + (size_t)pl.tail_units * kSoftmaxWarpsMax;
+    if (pl.rope_fused) n += 2 + (size_t)cdiv(b->total_new_tokens, kTcTileN);
+    return n;
+}
+
 Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     Plan pl;
     const bool tc = use_tensor_cores(p);
@@ -305,13 +316,16 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     // or 8 TMA boxes per operand, and pairs halve the boxes per FLOP.  The
     // one-pipeline kernel (attn_tc.cu) runs the rest -- block sizes 64 and
     // 128, decode-only batches (both measured faster on it), FP8 pools and
-    // the opt-in tail cut.  Pairs unless a batch of direct units only
-    // schedules better with single tiles (choose_tiles_per_unit, below).
+    // the opt-in tail cut, and the rotary embedding (which it applies in the
+    // same launch).  Pairs unless a batch of direct units only schedules
+    // better with single tiles (choose_tiles_per_unit, below).
     const int G = p->num_heads_q / p->num_heads_kv;
     bool pairs = false;
     for (int r = 0; r < b->num_reqs && !pairs; ++r)
         pairs = (long long)b->h_num_new_tokens[r] * G > kTcTileM;
-    pl.tc2 = tc && !kv_fp8(p) && !(p->flags & CPA_FLAG_TAIL_SPLIT) && p->block_size <= 32 && pairs;
+    const bool rope = p->rope_theta > 0.f;
+    pl.rope_fused = tc && !kv_fp8(p) && rope;
+    pl.tc2 = tc && !kv_fp8(p) && !rope && !(p->flags & CPA_FLAG_TAIL_SPLIT) && p->block_size <= 32 && pairs;
     pl.tiles_per_unit = pl.tc2 ? 2 : 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     // fewer, longer split units while the batch keeps enough of them: every
@@ -387,16 +401,20 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
         pl.qs_off = take(T * p->num_heads_q * sizeof(float));
         pl.kq_off = take(T * p->num_heads_kv * d);
         pl.vq_off = take(T * p->num_heads_kv * d);
+    } else if (pl.rope_fused) {
+        // the rotated copy of k_new, which the tensor-core kernel writes and
+        // reads (its queries are rotated in shared memory)
+        pl.rk_off = take(T * p->num_heads_kv * d * es);
     } else if (p->rope_theta > 0.f) {
         // rotated copies of q and k_new, which the attention then reads
         pl.rq_off = take(T * p->num_heads_q * d * es);
         pl.rk_off = take(T * p->num_heads_kv * d * es);
     }
     if (tc) {
-        // the persistent kernel's work counter and the tail units' counters,
-        // after the partials
+        // the persistent kernel's work counter, the tail units' counters and
+        // the key rotation's counters, after the partials
         pl.sched_off = (pl.ws_bytes + 255) & ~(size_t)255;
-        const size_t counters = sizeof(int) * (1 + (size_t)pl.tail_units * kSoftmaxWarpsMax);
+        const size_t counters = sizeof(int) * counter_ints(b, pl);
         pl.ws_bytes = pl.sched_off + ((counters + 255) & ~(size_t)255);
     }
     return pl;
@@ -582,7 +600,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool fuse_write = (params->flags & CPA_FLAG_FUSE_KV_WRITE) != 0;
     const float *q_rscale = nullptr;
-    const bool prepass = params->rope_theta > 0.f || kv_fp8(params);
+    const bool prepass = (params->rope_theta > 0.f && !pl.rope_fused) || kv_fp8(params);
     RopeArgs r{};
     if (prepass) {
         // pre-pass over the new rows: rotate q and k_new, encode the keys and
@@ -669,6 +687,17 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.k_scale = params->k_scale;
     a.v_scale = params->v_scale;
     a.q_rscale = q_rscale;
+    if (pl.rope_fused) {
+        // the kernel rotates the keys from the caller's k_new into the
+        // workspace copy, which then stands for k_new (its tiles, the write)
+        const RopeArgs ra = rope_args(batch, params, dev.err);
+        a.rope = 1;
+        a.rope_pieces = cdiv(batch->total_new_tokens, kRopePieceTokens);
+        a.k_src = k_new;
+        k_new = static_cast<char *>(workspace) + pl.rk_off;
+        a.k_new = k_new;
+        for (int c = 0; c < 64; ++c) a.turn_frac[c] = ra.turn_frac[c];
+    }
 
     cudaError_t e;
     if (pl.tile_m == kTcTileM) {
@@ -677,7 +706,8 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         if (prepass && launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;
         a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
         a.tail_count = pl.tail_units > 0 ? a.sched + 1 : nullptr;
-        e = cudaMemsetAsync(a.sched, 0, sizeof(int) * (1 + (size_t)pl.tail_units * kSoftmaxWarpsMax), st);
+        a.rope_count = pl.rope_fused ? a.sched + 1 + (size_t)pl.tail_units * kSoftmaxWarpsMax : nullptr;
+        e = cudaMemsetAsync(a.sched, 0, sizeof(int) * counter_ints(batch, pl), st);
         if (e == cudaSuccess) e = pl.tc2 ? launch_attn_tc2(a, maps, st) : launch_attn_tc(a, maps, st);
     } else {
         // the CUDA-core kernel (its pre-pass is RoPE only: FP8 pools need the

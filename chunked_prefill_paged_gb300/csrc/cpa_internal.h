@@ -54,6 +54,10 @@ constexpr int kFineTailWaves = 3;
 // 16-byte pieces of the new K/V rows per fused-write chunk of the tensor-core
 // kernel (each piece index copies 16 bytes of K and 16 bytes of V)
 constexpr int kWriteChunkPieces = 1024;
+// Tensor-core kernel with the rotary embedding: new tokens per piece of the
+// key rotation at the start of the launch (a 128-row tile of the new rows is
+// complete once its 128 / kRopePieceTokens pieces are).
+constexpr int kRopePieceTokens = 16;
 // Batches whose K/V (all requests, cached + new) exceed this many bytes walk
 // their direct units kv head by kv head (about half of GB300's L2).
 constexpr double kHeadMajorKvBytes = 64.0 * 1024 * 1024;
@@ -160,7 +164,26 @@ struct AttnArgs {
     const float *k_scale;  // [hkv]
     const float *v_scale;  // [hkv]
     const float *q_rscale; // [T, hq]
+    // Rotary embedding in the tensor-core kernel (BF16 pools): the queries are
+    // rotated in shared memory once their tile has landed; the new keys are
+    // rotated once, at the start of the launch, from k_src into k_new (a
+    // workspace copy that the new-key tiles and the fused write read).
+    // rope_count: [0] pieces claimed, [1] pieces done, [2 + i] pieces done of
+    // 128-row tile i of the new rows (zeroed before the launch).
+    int rope;
+    int rope_pieces;       // cdiv(total_tokens, kRopePieceTokens)
+    const void *k_src;     // [T, hkv, d] the caller's (unrotated) new keys
+    int *rope_count;
+    // turns per position of pair c, theta^(-2c/d) / (2 pi), as a 64-bit binary
+    // fraction (see RopeArgs)
+    unsigned long long turn_frac[64];
 };
+
+// Pieces of the key rotation that cover 128-row tile i of the new rows.
+CPA_HD int rope_pieces_of_tile(int total_tokens, int i) {
+    const int rows = total_tokens - i * kTcTileN;
+    return cdiv(rows < kTcTileN ? rows : kTcTileN, kRopePieceTokens);
+}
 
 // Piece length of request r's keys when its rows fit one tile.
 CPA_HD int split_len_of(const AttnArgs &a, int r) { return r >= a.fine_from ? a.split_len_fine : a.split_len; }

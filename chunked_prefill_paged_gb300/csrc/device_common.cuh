@@ -181,7 +181,7 @@ __device__ __forceinline__ void scatter_new_kv(const int32_t *cached, const int3
                                                int num_reqs, int max_blocks, int hkv, int bs, int num_blocks,
                                                int head_bytes, const void *k_new, const void *v_new,
                                                void *k_cache, void *v_cache, long long begin, long long end,
-                                               int stride_start, int stride, int *err) {
+                                               int stride_start, int stride, int *err, bool k_written = false) {
     const int pieces_per_head = head_bytes >> 4;
     const long long per_token = (long long)hkv * pieces_per_head;
     for (long long i = begin + stride_start; i < end; i += stride) {
@@ -195,7 +195,10 @@ __device__ __forceinline__ void scatter_new_kv(const int32_t *cached, const int3
         if (slot < 0) continue;
         const long long src = ((long long)t * hkv + g) * head_bytes + p * 16;
         const long long dst = (slot * hkv + g) * head_bytes + p * 16;
-        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + src));
+        // k_written: k_new was written earlier in this launch (the rotated
+        // keys), so it is read through the coherent path
+        const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + src);
+        const uint4 kv = k_written ? *ks : __ldg(ks);
         const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(v_new) + src));
         *reinterpret_cast<uint4 *>(static_cast<char *>(k_cache) + dst) = kv;
         *reinterpret_cast<uint4 *>(static_cast<char *>(v_cache) + dst) = vv;
@@ -214,6 +217,26 @@ __device__ __forceinline__ void fused_write_share(const AttnArgs &a, int cta, in
     if (b >= e) return;
     scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, head_bytes,
                    a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, nthreads, a.err);
+}
+
+// Rotary embedding ("Prefill Optimisation", section 2; the chunk's tokens
+// at their absolute positions, "Chunked Prefill"): pair (c, c + d/2) of a row
+// at position pos turns by the angle pos * theta^(-2c/d).  frac is that rate
+// in turns, theta^(-2c/d) / (2 pi), as a 64-bit binary fraction, so pos *
+// frac modulo 2^64 is the angle reduced to one turn; its top 24 bits, as the
+// exact float x in [0, 2) with angle = pi x, go to sincospif (whose own
+// reduction is exact, so no large-argument path).
+__device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long frac, float &c, float &s) {
+    const unsigned long long turn = (unsigned long long)pos * frac;  // wraps: modulo one turn
+    const float x = (float)(unsigned)(turn >> 40) * (1.0f / 8388608.0f);  // 2 * turns, exact
+    sincospif(x, &s, &c);
+}
+
+// (x0, x1) turned by the angle whose cosine and sine are (c, s), in fp32 with
+// a fixed rounding order, so every kernel that rotates a row gets the same bits
+__device__ __forceinline__ void rope_turn(float x0, float x1, float c, float s, float &y0, float &y1) {
+    y0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
+    y1 = __fmaf_rn(x1, c, __fmul_rn(x0, s));
 }
 
 __device__ __forceinline__ float to_float(float x) { return x; }

@@ -108,11 +108,7 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     for (int e = 0; e < PPL; ++e) {
         cs[e] = 1.f;
         sn[e] = 0.f;
-        if (a.rotate) {
-            const unsigned long long turn = (unsigned long long)pos * frac_s[lane * PPL + e];  // wraps: mod 1 turn
-            const float ang = (float)(turn >> 40) * (6.28318530717958648f / 16777216.0f);
-            sincosf(ang, &sn[e], &cs[e]);
-        }
+        if (a.rotate) rope_cos_sin(pos, frac_s[lane * PPL + e], cs[e], sn[e]);
     }
     long long slot = -1;
     if (a.write_pool) slot = slot_of(a.bt, a.max_blocks, a.bs, a.num_blocks, r, pos, a.err);
@@ -153,9 +149,10 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
         if (a.rotate) {
 #pragma unroll
             for (int e = 0; e < PPL; ++e) {
-                const float x0 = to_float(xl.e[e]), x1 = to_float(xh.e[e]);
-                xl.e[e] = from_float<T>(x0 * cs[e] - x1 * sn[e]);
-                xh.e[e] = from_float<T>(x1 * cs[e] + x0 * sn[e]);
+                float y0, y1;
+                rope_turn(to_float(xl.e[e]), to_float(xh.e[e]), cs[e], sn[e], y0, y1);
+                xl.e[e] = from_float<T>(y0);
+                xh.e[e] = from_float<T>(y1);
             }
         }
         if (is_q && a.q16) {

@@ -97,12 +97,24 @@ __device__ __forceinline__ void get_unit(Unit &u, const Unit &src) {
 // of the calling warp takes part): its index, and for an attention unit its
 // decoded fields in u.  The index is >= the unit count for a piece of the K/V
 // write or when the CTA is done; -1 when the wait gave up (timeout or abort).
+// With release = false the slot stays held (its fields valid) until
+// reread_unit(ring, i, u) copies them again and releases it.
 __device__ __forceinline__ int read_unit(UnitRing &ring, int i, long long limit, const volatile int *abort_flag,
-                                         Unit &u) {
+                                         Unit &u, bool release = true) {
     const int s = i % kUnitRing;
     if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&ring.full[s], (uint32_t)((i / kUnitRing) & 1), limit,
                                                          abort_flag)))
         return -1;
+    const int unit = *reinterpret_cast<volatile int *>(&ring.index[s]);
+    get_unit(u, ring.desc[s]);
+    __syncwarp();
+    if (release && (threadIdx.x & 31) == 0) ptx::mbar_arrive(&ring.empty[s]);
+    return unit;
+}
+
+// The unit of held slot i (read before with release = false), released now.
+__device__ __forceinline__ int reread_unit(UnitRing &ring, int i, Unit &u) {
+    const int s = i % kUnitRing;
     const int unit = *reinterpret_cast<volatile int *>(&ring.index[s]);
     get_unit(u, ring.desc[s]);
     __syncwarp();

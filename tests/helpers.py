@@ -23,6 +23,13 @@ BF16_REL_RMS = 1e-2  # gate on the relative RMS error of each checked step
 # softmax is peaked (the peaky and needle input variants).
 BF16_ROW_REL = 2e-2
 FP32_ROW_REL = 1e-3
+# A BF16 output is stored rounded to bf16: half an ulp, up to 2^-8 |o|.  The
+# max-abs bound is applied to the error beyond that rounding, |o - o_ref| <=
+# 2e-2 + 2^-8 |o_ref| per element: at |o| >= 4 half an ulp alone is 2^-6, and
+# a result whose fp32 value lies near a rounding midpoint (P itself rounded to
+# bf16 before the PV product moves it by up to 2^-9 relative) lands one ulp,
+# 2^-5, from the exact value.  Below |o| = 0.5 the allowance is under 2e-3.
+BF16_ROUNDING_REL = 2.0 ** -8
 
 
 def to_oracle(t: torch.Tensor) -> np.ndarray:
@@ -69,6 +76,7 @@ def sample_rows(step: W.Step, n_per_req: int, seed: int) -> List[int]:
 class Result:
     def __init__(self):
         self.max_err = 0.0
+        self.max_err_beyond_bf16 = 0.0  # max of |o - o_ref| - 2^-8 |o_ref|
         self.max_lse_err = 0.0
         self.rel_rms = []
         self.max_row_rel = 0.0
@@ -79,6 +87,8 @@ class Result:
         err = np.abs(gpu_out.astype(np.float64) - ref_out)
         self.max_err = max(self.max_err, float(err.max()) if err.size else 0.0)
         if err.size:
+            self.max_err_beyond_bf16 = max(self.max_err_beyond_bf16,
+                                           float((err - BF16_ROUNDING_REL * np.abs(ref_out)).max()))
             self.rel_rms.append(float(np.sqrt((err ** 2).mean()) / max(np.sqrt((ref_out ** 2).mean()), 1e-30)))
             e_row = np.sqrt((err ** 2).sum(axis=-1))
             r_row = np.sqrt((ref_out.astype(np.float64) ** 2).sum(axis=-1))
@@ -138,10 +148,13 @@ def gate_failures(res: Result, dtype: str) -> List[str]:
     bad = []
     if dtype == "f32":
         atol, lse_tol, row_tol = FP32_ATOL, FP32_LSE_ATOL, FP32_ROW_REL
+        if not res.max_err <= atol:
+            bad.append(f"max-abs error {res.max_err:.3e} > {atol}")
     else:
         atol, lse_tol, row_tol = BF16_ATOL, BF16_LSE_ATOL, BF16_ROW_REL
-    if not res.max_err <= atol:
-        bad.append(f"max-abs error {res.max_err:.3e} > {atol}")
+        if not res.max_err_beyond_bf16 <= atol:
+            bad.append(f"max-abs error beyond the bf16 rounding {res.max_err_beyond_bf16:.3e} > {atol} "
+                       f"(max-abs {res.max_err:.3e})")
     if not res.max_lse_err <= lse_tol:
         bad.append(f"lse error {res.max_lse_err:.3e} > {lse_tol}")
     if not res.max_row_rel <= row_tol:

@@ -4,7 +4,7 @@
 // the kernel launchers it refers to are stubs (nothing here touches a GPU).
 //
 // stdin: sms hq hkv d bs kv_segment_size dtype flags kv_format num_reqs, then
-// num_reqs pairs (cached_seq_len num_new_tokens).
+// num_reqs pairs (cached_seq_len num_new_tokens), then optionally rope_theta.
 #include "../chunked_prefill_paged_gb300/csrc/cpa_api.cu"
 
 #include <stdio.h>
@@ -31,6 +31,8 @@ int main() {
         total += N[r];
         longest = C[r] + N[r] > longest ? C[r] + N[r] : longest;
     }
+    float rope_theta = 0.f;
+    if (scanf("%f", &rope_theta) != 1) rope_theta = 0.f;
     cpa_batch b{};
     b.num_reqs = n;
     b.max_blocks_per_seq = (longest + bs - 1) / bs;
@@ -48,13 +50,15 @@ int main() {
     p.dtype = dtype;
     p.flags = flags;
     p.kv_format = kv_format;
+    p.rope_theta = rope_theta;
     const cpa::Plan pl = cpa::make_plan(&b, &p, sms);
     printf("{\"split_len\": %d, \"split_len_fine\": %d, \"fine_from\": %d, \"fine_units\": %d, "
            "\"direct_units\": %d, \"split_units\": %d, \"split_reqs\": %d, \"tail_units\": %d, \"tail_pieces\": %d, "
            "\"head_major\": %d, \"interleave_span\": %d, \"ws_bytes\": %zu, \"sched_off\": %zu, "
-           "\"tiles_per_unit\": %d, \"tc2\": %d}\n",
+           "\"tiles_per_unit\": %d, \"tc2\": %d, \"rope_fused\": %d}\n",
            pl.split_len, pl.split_len_fine, pl.fine_from == INT32_MAX ? -1 : pl.fine_from, pl.fine_units,
            pl.direct_units, pl.split_units, pl.split_reqs, pl.tail_units, pl.tail_pieces, pl.head_major,
-           pl.direct_units + pl.split_units - pl.fine_units, pl.ws_bytes, pl.sched_off, pl.tiles_per_unit, pl.tc2 ? 1 : 0);
+           pl.direct_units + pl.split_units - pl.fine_units, pl.ws_bytes, pl.sched_off, pl.tiles_per_unit, pl.tc2 ? 1 : 0,
+           pl.rope_fused ? 1 : 0);
     return 0;
 }

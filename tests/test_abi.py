@@ -154,8 +154,13 @@ def test_workspace_size_counts_rotated_copies(lib):
     p = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0).c()
     rq = 512 * 32 * 128 * 2   # rotated queries, bf16
     rk = 512 * 8 * 128 * 2    # rotated new keys
-    # the copies come first (256-byte aligned), the work counter stays last
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + rk + plain
+    # tensor-core kernel: the queries are rotated in shared memory, so only the
+    # keys' copy comes first (256-byte aligned); the counters stay last (the
+    # work counter and the rotation's 2 + 4 counts fit the same 256 bytes)
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rk + plain
+    # the CUDA-core kernel (forced) reads rotated copies of both, and keeps no counter
+    ps = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0, flags=lib.FLAG_FORCE_SIMT).c()
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(ps)) == rq + rk
 
 
 def _fp8_params(lib, k_scale=0x1000, v_scale=0x1000, **kw):

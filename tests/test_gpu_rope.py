@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import BF16_ATOL, FP32_ATOL, Result, assert_within, bits, params_for, to_oracle
+from helpers import BF16_ATOL, FP32_ATOL, Result, assert_within, bits, params_for, sample_rows, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -145,3 +145,72 @@ def test_rope_chunked_prompt_matches_oracle(cpa):
                                              head_dim=128, block_size=16)
     assert cpa.last_device_error() == cpa.SUCCESS
     assert_within(res, "bf16")
+
+
+def run_rope(cpa, w, *, flags=None, rows_per_req=None, steps_to_check=None, variant="plain", seed=0):
+    """Every step of `w` with the rotary embedding applied in the call (fused
+    write unless flags say otherwise, then the standalone write): outputs of
+    the checked steps (all rows, or a sample) against the oracle's rotation
+    rounded to bf16 then attention in fp64; after each step the pool's keys
+    within one rounding step of the oracle's rotated keys and its values
+    bit-exact."""
+    sh = w.shape
+    t = w.materialize("cuda")
+    W.apply_variant(t, variant, sh.num_heads_q // sh.num_heads_kv)
+    fl = cpa.FLAG_FUSE_KV_WRITE if flags is None else flags
+    p = rope_params(w, fl)
+    k_pool_o, v_pool_o = as_f64(t.k_cache), as_f64(t.v_cache)
+    steps_to_check = range(len(w.steps)) if steps_to_check is None else steps_to_check
+    res = Result()
+    for si, s in enumerate(w.steps):
+        b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+        q, kn, vn = t.step_inputs(s)
+        out, lse = cpa.attention(b, p, q, kn, vn, t.k_cache, t.v_cache)
+        if not fl & cpa.FLAG_FUSE_KV_WRITE:
+            cpa.paged_kv_write(b, p, kn, vn, t.k_cache, t.v_cache)
+        torch.cuda.synchronize()
+        assert cpa.last_device_error() == cpa.SUCCESS
+        ob = oracle.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+        qr, kr = oracle.rope(ob, as_f64(q), as_f64(kn), num_heads_q=sh.num_heads_q, num_heads_kv=sh.num_heads_kv,
+                             head_dim=sh.head_dim, theta=THETA)
+        qr, kr = rounded(qr, "bf16"), rounded(kr, "bf16")
+        if si in steps_to_check:
+            rows = None if rows_per_req is None else sample_rows(s, rows_per_req, seed + si)
+            ref_o, ref_l = oracle.attention(ob, qr, kr, as_f64(vn), k_pool_o, v_pool_o,
+                                            num_heads_q=sh.num_heads_q, num_heads_kv=sh.num_heads_kv,
+                                            head_dim=sh.head_dim, block_size=sh.block_size, scale=sh.scale,
+                                            rows=rows)
+            idx = slice(None) if rows is None else torch.as_tensor(rows, device=out.device)
+            res.add(out[idx].float().cpu().numpy(), ref_o, lse[idx].cpu().numpy(), ref_l)
+        check_pool_keys(t.k_cache, t.v_cache, s, w.block_table, kr, vn, sh.block_size, "bf16")
+        k_pool_o, v_pool_o = oracle.kv_write(ob, kr, as_f64(vn), k_pool_o, v_pool_o, num_heads_kv=sh.num_heads_kv,
+                                             head_dim=sh.head_dim, block_size=sh.block_size)
+    assert_within(res, "bf16")
+
+
+# Tensor-core shapes with the rotation applied in the attention launch: G = 1
+# (every row its own token), G = 16 and 32 (few tokens per query tile), head
+# dimension 64 (both halves of a pair in one 128-byte row); prefills with and
+# without cached keys, a ragged chunk and decodes (split units) side by side.
+@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 8, 128, 16), (16, 1, 128, 128), (8, 2, 64, 16), (64, 2, 128, 32)])
+def test_rope_tensor_core_shapes(cpa, hq, hkv, d, bs):
+    reqs = [(0, 300), (130, 77), (1000, 1), (257, 129), (4000, 1)]
+    w = W.make_batch_workload(f"rope_tc_{hq}_{hkv}_{d}_{bs}", W.Shape(hq, hkv, d, bs, 512, "bf16"), reqs, seed=44)
+    run_rope(cpa, w)
+
+
+def test_rope_without_fused_write_and_with_tail_pieces(cpa):
+    # no fused write: the rotated keys are only read (the standalone write
+    # follows); then the opt-in tail cut, whose pieces each rotate their queries
+    reqs = [(0, 700), (3000, 900), (50, 1)]
+    w = W.make_batch_workload("rope_tail", W.Shape(32, 8, 128, 16, 1024, "bf16"), reqs, seed=45)
+    run_rope(cpa, w, flags=0)
+    run_rope(cpa, w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_TAIL_SPLIT)
+
+
+def test_rope_llama3_8b_prompt_sampled(cpa):
+    # the 10,000-token prompt in 5 chunks of 2048 with theta 5e5, sharpened
+    # queries: the first chunk (every key new: query tiles wait for the
+    # rotation of their keys) and the last (8,192 cached keys) on sampled rows
+    w = W.llama3_8b_prompt()
+    run_rope(cpa, w, rows_per_req=24, steps_to_check=[0, 4], variant="peaky", seed=7)

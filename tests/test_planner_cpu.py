@@ -44,9 +44,9 @@ def harness(tmp_path_factory):
     return exe
 
 
-def plan(harness, reqs, sms=152, hq=32, hkv=8, d=128, bs=16, seg=1024, flags=FUSE, kv_format=0):
+def plan(harness, reqs, sms=152, hq=32, hkv=8, d=128, bs=16, seg=1024, flags=FUSE, kv_format=0, rope=0.0):
     text = f"{sms} {hq} {hkv} {d} {bs} {seg} 1 {flags} {kv_format} {len(reqs)}\n"
-    text += "\n".join(f"{c} {n}" for c, n in reqs) + "\n"
+    text += "\n".join(f"{c} {n}" for c, n in reqs) + f"\n{rope}\n"
     out = subprocess.run([harness], input=text, capture_output=True, text=True, check=True).stdout
     return json.loads(out)
 
@@ -230,3 +230,10 @@ def test_kernel_choice(harness):
     assert plan(harness, [(8192, 1)] * 8, bs=16)["tc2"] == 0
     assert plan(harness, [(30720, 2048)], bs=16, kv_format=1)["tc2"] == 0
     assert plan(harness, [(30720, 2048)], bs=16, flags=FUSE | TAIL_SPLIT)["tc2"] == 0
+    # the rotary embedding: the one-pipeline kernel, which applies it in the
+    # same launch (BF16 pools); FP8 pools keep the pre-pass
+    got = plan(harness, [(30720, 2048)], bs=16, rope=500000.0)
+    assert (got["tc2"], got["rope_fused"], got["tiles_per_unit"]) == (0, 1, 1)
+    assert plan(harness, [(8192, 1808)], bs=128, rope=500000.0)["rope_fused"] == 1
+    assert plan(harness, [(8192, 1808)], bs=128, kv_format=1, rope=500000.0)["rope_fused"] == 0
+    assert plan(harness, [(8192, 1808)], bs=128)["rope_fused"] == 0
