@@ -41,6 +41,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -373,12 +374,13 @@ def run_ours(args, rank, world, local):
 
     host_copies = pinned_copy_rates(dev, h2d, d2h, e2e_ms / args.steps)
 
-    secondary = fp8_mixed = prefix = long_last = None
+    secondary = fp8_mixed = prefix = long_last = rope = None
     if not args.no_secondary:
         secondary = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush)
         fp8_mixed = run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=True)
         prefix = run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, W.prefix_cache, 0)
         long_last = run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, W.long_context, -1)
+        rope = run_rope_overhead(args, dev, stream, flush)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -402,6 +404,7 @@ def run_ours(args, rank, world, local):
         "fp8_mixed": fp8_mixed,
         "prefix_cache": prefix,
         "long_context_last": long_last,
+        "rope_last_chunk": rope,
     }
     return line
 
@@ -456,6 +459,50 @@ def warm_cache(cpa, w, t, params, dev, upto):
         cpa.paged_kv_write(b, params, k, v, t.k_cache, t.v_cache)
 
 
+def tc_kernel_name(sh, step, rope=False, fp8=False):
+    """The tensor-core kernel the library's planner picks for this batch (its
+    rule, restated for labelling): the two-pipeline kernel for BF16 pools at
+    block sizes up to 32 with query tiles to pair and no rotary embedding."""
+    G = sh.num_heads_q // sh.num_heads_kv
+    pairs = any(int(n) * G > 128 for n in step.num_new_tokens)
+    if not fp8 and not rope and sh.block_size <= 32 and pairs:
+        return f"attn_tc2_kernel<{sh.head_dim}>"
+    return f"attn_tc_kernel<{sh.head_dim}, {'true' if fp8 else 'false'}>"
+
+
+def time_prefill_calls(args, dev, stream, flush, w, t, i, thetas):
+    """Median CUDA-event time (ms) of one attention call of step i for each
+    rope_theta in `thetas`, the calls of the different thetas interleaved
+    (each after an L2 flush)."""
+    import chunked_prefill_paged_gb300 as cpa
+    sh = w.shape
+    s = w.steps[i]
+    plist = [cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE, rope_theta=th)
+             for th in thetas]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
+    q, k, v = t.step_inputs(s)
+    out = torch.empty_like(q)
+    n = max(cpa.workspace_size(b, p) for p in plist)
+    ws = torch.empty(max(n // 4, 4), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        for p in plist:
+            cpa.chunked_prefill_attention(b, p, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+    torch.cuda.synchronize(dev)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in plist]
+           for _ in range(args.steps)]
+    for row in evs:
+        for p, (e0, e1) in zip(plist, row):
+            flush.zero_()
+            e0.record(stream)
+            cpa.chunked_prefill_attention(b, p, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
+            e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if cpa.last_device_error(stream) != cpa.SUCCESS:
+        raise RuntimeError(f"device error in {w.name}")
+    return [statistics.median(row[j][0].elapsed_time(row[j][1]) for row in evs) for j in range(len(plist))]
+
+
 def run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, make, idx):
     """A prefill-heavy configuration's attention call (one workload step,
     its cache holding the earlier chunks' K/V): algorithmic TFLOP/s against
@@ -469,24 +516,7 @@ def run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, make, idx)
     params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
                         sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
     warm_cache(cpa, w, t, params, dev, i)
-    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table, device=dev)
-    q, k, v = t.step_inputs(s)
-    out = torch.empty_like(q)
-    n = cpa.workspace_size(b, params)
-    ws = torch.empty(max(n // 4, 4), dtype=torch.float32, device=dev)
-    for _ in range(max(args.warmup, 3)):
-        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
-    torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        cpa.chunked_prefill_attention(b, params, q, k, v, t.k_cache, t.v_cache, out, None, ws, stream)
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if cpa.last_device_error(stream) != cpa.SUCCESS:
-        raise RuntimeError(f"device error in {w.name}")
-    ms = statistics.median(a.elapsed_time(b_) for a, b_ in evs)
+    (ms,) = time_prefill_calls(args, dev, stream, flush, w, t, i, [0.0])
     flops = w.flops_per_step()[i]
     achieved = flops / (ms / 1e3) / 1e12
     del t
@@ -497,8 +527,29 @@ def run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, make, idx)
             "launches_per_step": 1,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
-                         "traffic": None, "kernel": "attn_tc_kernel<128, false>"},
+                         "traffic": None, "kernel": tc_kernel_name(sh, s)},
             "l2": "flushed before every timed call (256 MiB write)"}
+
+
+def run_rope_overhead(args, dev, stream, flush, theta=500000.0):
+    """The Llama prompt's last chunk (cached 8192) with the rotary embedding
+    applied in the call against the same call without it, interleaved."""
+    import chunked_prefill_paged_gb300 as cpa
+    w = W.llama3_8b_prompt()
+    sh = w.shape
+    t = w.materialize(dev, sentinel=W.SENTINEL_ZERO)
+    i = len(w.steps) - 1
+    params = cpa.Params(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size, w.num_blocks,
+                        sh.kv_segment_size, sh.scale, cpa.DTYPE_BF16, cpa.FLAG_FUSE_KV_WRITE)
+    warm_cache(cpa, w, t, params, dev, i)
+    steps = types.SimpleNamespace(steps=max(args.steps, 20), warmup=args.warmup)
+    ms_plain, ms_rope = time_prefill_calls(steps, dev, stream, flush, w, t, i, [0.0, theta])
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "step": i, "rope_theta": theta, "ms_no_rope": round(ms_plain, 4),
+            "ms_rope": round(ms_rope, 4), "overhead": round(ms_rope / ms_plain - 1.0, 4),
+            "kernel": tc_kernel_name(sh, w.steps[i], rope=True), "calls_each": steps.steps,
+            "how": "median of interleaved calls, each after a 256 MiB L2 flush"}
 
 
 def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=False):

@@ -237,3 +237,21 @@ def test_kernel_choice(harness):
     assert plan(harness, [(8192, 1808)], bs=128, rope=500000.0)["rope_fused"] == 1
     assert plan(harness, [(8192, 1808)], bs=128, kv_format=1, rope=500000.0)["rope_fused"] == 0
     assert plan(harness, [(8192, 1808)], bs=128)["rope_fused"] == 0
+
+
+def test_bench_kernel_labels_follow_the_planner(harness):
+    # bench.py names the kernel of each prefill line by restating the
+    # planner's choice; the planner itself decides here
+    import bench
+    import workloads as W
+    for make, idx in [(W.prefix_cache, 0), (W.long_context, -1), (W.llama3_8b_prompt, -1), (W.mixed_step, 0)]:
+        w = make()
+        sh = w.shape
+        s = w.steps[idx]
+        reqs = list(zip((int(c) for c in s.cached_seq_len), (int(n) for n in s.num_new_tokens)))
+        got = plan(harness, reqs, hq=sh.num_heads_q, hkv=sh.num_heads_kv, d=sh.head_dim, bs=sh.block_size,
+                   seg=sh.kv_segment_size)
+        assert bench.tc_kernel_name(sh, s).startswith("attn_tc2_kernel") == bool(got["tc2"]), w.name
+        got_rope = plan(harness, reqs, hq=sh.num_heads_q, hkv=sh.num_heads_kv, d=sh.head_dim, bs=sh.block_size,
+                        seg=sh.kv_segment_size, rope=500000.0)
+        assert bench.tc_kernel_name(sh, s, rope=True).startswith("attn_tc2_kernel") == bool(got_rope["tc2"])
