@@ -48,8 +48,10 @@
 //              also rotate each unit's query tile in its Q stage once it has
 //              landed, one unit ahead of the outputs, and the score MMAs wait
 //              for that (q_rot) instead of the copy.
-//   warps 12-15 (FP8 pools) expand E4M3 code tiles in place into the
-//              fp16 tiles the MMAs read (K: 12-13, V: 14-15).
+//   warps 12-15 (FP8 pools) expand E4M3 value code tiles in place into the
+//              fp16 tiles the PV MMAs read (32 rows each).  The score MMAs read
+//              the key codes as they landed (E4M3 operands, .kind::f8f6f4), with
+//              the queries as two E4M3 planes (a row and its rounding residual).
 //
 // TMEM (512 columns): three score buffers S0 [0,128), S1 [128,256) and
 // S2 [256,384), O [384, 384 + D).  P(j), as bf16 (fp16) pairs, overwrites the first
@@ -123,9 +125,10 @@ struct TcCfg {
     static constexpr int kQStages = F8 ? 1 : 2;
     static constexpr int kKStages = (D == 128) ? 3 : 6;
     static constexpr int kVStages = (D == 128) ? (F8 ? 3 : 2) : 5;
-    // FP8 pools: a K / V copy brings a code tile (128 rows x D bytes) into the
-    // upper half of its ring slot, and the expansion warps turn it in place
-    // into the 16-bit tile the MMAs read
+    // FP8 pools: a K copy brings a code tile (128 rows x D bytes, 128-byte
+    // swizzled) to the start of its ring slot, where the score MMA reads it;
+    // a V copy brings one (plain rows) into the upper half of its slot, and
+    // the expansion warps turn it in place into the fp16 tile the PV MMA reads
     static constexpr int kCodeTileBytes = 128 * D;
     static constexpr int kSmemBytes = 1024 /*align*/ + kTileBytes * (kQStages + kKStages + kVStages);
 };
@@ -144,7 +147,7 @@ struct __align__(8) TcShared {
     // sums to the epilogue warps (epi_full), which free the arrays once read
     uint64_t epi_full, epi_empty;
     float epi_m[128], epi_l[128];
-    uint64_t k8_full[6], v8_full[6];  // FP8 pools: a slot's code tile has landed
+    uint64_t v8_full[6];  // FP8 pools: a V slot's code tile has landed
     // unit scheduler: warp 8 takes unit indices from the launch's work
     // counter and passes them to the other roles through this ring
     UnitRing ring;
@@ -163,32 +166,30 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(b));
 }
 
-// Rows [r0, r0 + 64) of a 128 x 128 code tile, held in the upper half of its
+// Rows [r0, r0 + 32) of a 128 x 128 code tile, held in the upper half of its
 // ring slot (rows of 128 bytes at slot + 16 KB), expanded in place into the
 // 16-bit tile the MMAs read: two 64-column halves of 128 rows x 128 B at
 // slot and slot + 16 KB, 16-byte chunk c of row r at chunk position
 // c ^ (r % 8) (the 128-byte swizzle).  Half 1 of row r overwrites code row r
 // only, so reading each row before writing it keeps the expansion in place;
-// a batch of eight rows per lane is read before any of them is written (the
-// loads then overlap), and the two warps of a tile own disjoint rows.
-// Rows at or past `valid` become zeros when zero_tail is set (code 0), else
-// they are left as they are.  Eight lanes share a row: lane piece p (16
+// the eight rows of each lane are read before any of them is written (the
+// loads then overlap), and the four warps of a tile own disjoint rows.
+// Rows at or past `valid` become zeros (code 0).  Eight lanes share a row: lane piece p (16
 // codes, columns 16p .. 16p + 15) fills chunks 2(p % 4) and 2(p % 4) + 1 of
 // half p / 4.  Which of its two chunks a lane handles first alternates with
 // the half and with the row's parity: then every store instruction covers all
 // eight chunk positions of each row, and every 8-byte load instruction reads
 // row pairs whose byte ranges fall on complementary banks -- neither
 // conflicts.
-__device__ __forceinline__ void expand_code_rows(uint8_t *slot, int r0, int valid, bool zero_tail, int lane,
-                                                 int half_bytes) {
+__device__ __forceinline__ void expand_code_rows(uint8_t *slot, int r0, int valid, int lane, int half_bytes) {
     const uint8_t *codes = slot + half_bytes;
     const int p = lane & 7;
     const int h = p >> 2;
     const int f = h ^ ((lane >> 3) & 1);  // r0 is even, so (lane >> 3) & 1 is the row's parity
     const int c_first = 2 * (p & 3) + f, c_second = 2 * (p & 3) + 1 - f;
-    constexpr int kBatch = 8;
-#pragma unroll 1
-    for (int it0 = 0; it0 < 16; it0 += kBatch) {
+    constexpr int kBatch = 8;  // 8 x 4 = 32 rows, every load before any store
+    {
+        const int it0 = 0;
         uint2 w0[kBatch], w1[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
@@ -204,7 +205,6 @@ __device__ __forceinline__ void expand_code_rows(uint8_t *slot, int r0, int vali
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
             const int r = r0 + (it0 + i) * 4 + (lane >> 3);
-            if (r >= valid && !zero_tail) continue;
             uint4 o0, o1;
             e4m3x4_to_f16(w0[i].x, o0.x, o0.y);
             e4m3x4_to_f16(w0[i].y, o0.z, o0.w);
@@ -490,12 +490,11 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // 16-bit tiles: filled by one TMA arrival, or (FP8 pools) by the two
         // expansion warps once the code tile's copies (k8 / v8_full) landed
         for (int s = 0; s < NSK; ++s) {
-            mbar_init(&sh.k_full[s], F8 ? 2 : 1);
+            mbar_init(&sh.k_full[s], 1);
             mbar_init(&sh.k_empty[s], 1);
-            mbar_init(&sh.k8_full[s], 1);
         }
         for (int s = 0; s < NSV; ++s) {
-            mbar_init(&sh.v_full[s], F8 ? 2 : 1);
+            mbar_init(&sh.v_full[s], F8 ? 4 : 1);
             mbar_init(&sh.v_empty[s], 1);
             mbar_init(&sh.v8_full[s], 1);
         }
@@ -537,12 +536,13 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // ================================================================ TMA
         const int kv_role = (warp == kVProducerWarp) ? 1 : 0;  // copies K (0) or V (1)
         bool ok = true;
-        // the copies' ring; with FP8 pools a code tile goes to the upper half
-        // of its slot and its own barrier (the expansion then fills the slot)
+        // the copies' ring; with FP8 pools a value code tile goes to the upper
+        // half of its slot and its own barrier (the expansion then fills the
+        // slot), a key code tile to the start of its slot
         const int ns = kv_role ? NSV : NSK;
-        uint64_t *const ring_full = F8 ? (kv_role ? sh.v8_full : sh.k8_full) : (kv_role ? sh.v_full : sh.k_full);
+        uint64_t *const ring_full = kv_role ? (F8 ? sh.v8_full : sh.v_full) : sh.k_full;
         uint64_t *const ring_empty = kv_role ? sh.v_empty : sh.k_empty;
-        uint8_t *const ring = (kv_role ? sV : sK) + (F8 ? HB : 0);
+        uint8_t *const ring = kv_role ? sV + (F8 ? HB : 0) : sK;
         constexpr int slot_bytes = F8 ? CB : TB;
         int slot = 0;         // ring slot of the next copy
         uint32_t ph = 0;      // parity of that slot's current fill
@@ -710,9 +710,14 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     }
                     if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qb], TB);
                     __syncwarp();
-                    if (lane < Cfg::kHalves)
-                        tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, uq.g * a.G,
-                                    uq.cu0 + uq.row0 / a.G);
+                    const int tok0 = uq.cu0 + uq.row0 / a.G;
+                    if (F8) {
+                        // the two E4M3 planes of the queries
+                        if (lane < 2)
+                            tma_load_4d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], 0, uq.g * a.G, tok0, lane);
+                    } else if (lane < Cfg::kHalves) {
+                        tma_load_3d(sQ + qb * TB + lane * HB, &tm_q, &sh.q_full[qb], lane * 64, uq.g * a.G, tok0);
+                    }
                     return true;
                 };
                 if (ok && !(early == it && early_q) && !copy_q(it, u, true)) ok = false;
@@ -792,7 +797,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         bool ok = true;
         // bf16 operands; fp16 with FP8 pools (queries scaled per row, codes
         // expanded exactly, probabilities rounded to fp16)
-        constexpr uint32_t idesc_s = idesc_16bit_f32(128, kKT, 0, 0, !F8);
+        constexpr uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, kKT) : idesc_16bit_f32(128, kKT, 0, 0, true);
         constexpr uint32_t idesc_pv = idesc_16bit_f32(128, D, 0, 1, !F8);
         // Shared-memory descriptors: the high halves (stride, version,
         // swizzle) are common to Q, K and V; only the low halves (start
@@ -843,7 +848,9 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     tc_fence_after();
                     const uint32_t k_lo = k_lo0 + (uint32_t)rs * (uint32_t)(TB >> 4);
                     const uint32_t d_tmem = tmem + ub * kKT;
-                    if constexpr (D == 128) {
+                    if constexpr (F8) {
+                        umma_s_tile_e4m3(d_tmem, q_lo_u, k_lo, desc_hi, idesc_s, (uint32_t)(HB >> 4));
+                    } else if constexpr (D == 128) {
                         umma_s_tile128(d_tmem, q_lo_u, k_lo, desc_hi, idesc_s, (uint32_t)(HB >> 4));
                     } else {
 #pragma unroll
@@ -1101,14 +1108,12 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         }
     } else if (F8 && warp >= kKConvWarp) {
         // ==================================== FP8 expansion (warps 12-15)
-        // Warps 12-13 expand K code tiles, 14-15 V tiles, in their ring slots;
-        // each warp takes 64 rows.  V rows past a tile's valid keys become
-        // zeros (P = 0 must not meet a NaN code left in the pool or a stale
-        // value); K rows there are left as they are, the softmax masks their
-        // scores.
-        const int kv = (warp - kKConvWarp) >> 1;
-        const int r0 = ((warp - kKConvWarp) & 1) * 64;
-        const int nsb = kv ? NSV : NSK;
+        // Warp 12 + w expands rows 32w .. 32w + 31 of every V code tile in its
+        // ring slot.  V rows past a tile's valid keys become zeros (P = 0 must
+        // not meet a NaN code left in the pool or a stale value).  Key code
+        // rows there are left as they are: the softmax masks their scores.
+        const int r0 = (warp - kKConvWarp) * 32;
+        const int nsb = NSV;
         int sb = 0;
         uint32_t phb = 0;
         bool ok = true;
@@ -1125,8 +1130,8 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
             TileList tl;
             tl.init(u);
             for (int j = 0; j < tl.n_total; ++j) {
-                uint64_t *code_full = kv ? &sh.v8_full[sb] : &sh.k8_full[sb];
-                uint64_t *tile_full = kv ? &sh.v_full[sb] : &sh.k_full[sb];
+                uint64_t *code_full = &sh.v8_full[sb];
+                uint64_t *tile_full = &sh.v_full[sb];
                 if (!__all_sync(0xffffffffu, mbar_wait_or_abort(code_full, phb, LIM, abort_flag))) {
                     ok = false;
                     break;
@@ -1134,7 +1139,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 int key0, valid;
                 bool pooled;
                 tl.tile(j, key0, valid, pooled);
-                expand_code_rows((kv ? sV : sK) + sb * TB, r0, valid, kv == 1, lane, HB);
+                expand_code_rows(sV + sb * TB, r0, valid, lane, HB);
                 fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tile_full);

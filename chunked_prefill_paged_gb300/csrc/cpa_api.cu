@@ -132,7 +132,7 @@ struct Plan {
     size_t sched_off = 0;   // byte offset of the work counter in the workspace
     size_t rq_off = 0, rk_off = 0;  // rotated q / k_new copies (rope_theta > 0)
     size_t kq_off = 0, vq_off = 0;  // FP8 cache: codes of k_new / v_new
-    size_t q16_off = 0, qs_off = 0; // FP8 cache: fp16 queries and their row scales
+    size_t q8_off = 0, qs_off = 0;  // FP8 cache: two E4M3 planes of the queries, their row scales
     size_t ws_bytes = 0;    // workspace bytes: partials, then (tensor-core path) the counter
     int split_len = 0;
     int split_len_fine = 0;
@@ -395,9 +395,9 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
         return off;
     };
     if (kv_fp8(p)) {
-        // the (rotated) queries as fp16 with their row scales, and the new rows
-        // as the FP8 cache holds them, which the attention then reads
-        pl.q16_off = take(T * p->num_heads_q * d * 2);
+        // the (rotated) queries as two E4M3 planes with their row scales, and
+        // the new rows as the FP8 cache holds them, which the attention reads
+        pl.q8_off = take(2 * T * p->num_heads_q * d);
         pl.qs_off = take(T * p->num_heads_q * sizeof(float));
         pl.kq_off = take(T * p->num_heads_kv * d);
         pl.vq_off = take(T * p->num_heads_kv * d);
@@ -421,23 +421,24 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
 }
 
 
-// 16-bit tiles land 128-byte swizzled (the MMA operand layout); FP8 code
-// tiles land as plain rows for the expansion warps
-enum class MapType { kBf16, kF16, kCodes };
+// 16-bit tiles land 128-byte swizzled (the MMA operand layout), as do the
+// E4M3 tiles the score MMA reads (kCodesMma: query planes, key codes); value
+// code tiles land as plain rows for the expansion warps (kCodes)
+enum class MapType { kBf16, kF16, kCodes, kCodesMma };
 
 cpa_status encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                   const cuuint32_t *box, MapType type = MapType::kBf16) {
     auto enc = tensor_map_encoder();
     if (!enc) return CPA_ERR_CUDA;
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    const bool codes = type == MapType::kCodes;
+    const bool codes = type == MapType::kCodes || type == MapType::kCodesMma;
     const CUtensorMapDataType dt = codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : type == MapType::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = enc(map, dt, (cuuint32_t)rank,
                      const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     type == MapType::kCodes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? CPA_SUCCESS : CPA_ERR_CUDA;
 }
 
@@ -446,13 +447,18 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
     const cuuint64_t D = (cuuint64_t)p->head_dim, Hq = (cuuint64_t)p->num_heads_q, Hkv = (cuuint64_t)p->num_heads_kv;
     const cuuint64_t T = (cuuint64_t)b->total_new_tokens, bs = (cuuint64_t)p->block_size;
     const cuuint32_t G = (cuuint32_t)(p->num_heads_q / p->num_heads_kv);
-    {
+    if (kv_fp8(p)) {
+        // with the FP8 cache q is the pre-pass's two E4M3 planes [2][T, H_q, d]:
+        // a box is one plane's (d bytes, G heads, 128 / G tokens)
+        const cuuint64_t dims[4] = {D, Hq, T, 2};
+        const cuuint64_t strides[3] = {D, Hq * D, T * Hq * D};
+        const cuuint32_t box[4] = {(cuuint32_t)D, G, (cuuint32_t)kTcTileM / G, 1};
+        if (cpa_status s = encode(&m.q, q, 4, dims, strides, box, MapType::kCodesMma)) return s;
+    } else {
         const cuuint64_t dims[3] = {D, Hq, T};
         const cuuint64_t strides[2] = {D * 2, Hq * D * 2};
         const cuuint32_t box[3] = {64, G, (cuuint32_t)kTcTileM / G};
-        // with the FP8 cache q is the pre-pass's fp16 copy
-        if (cpa_status s = encode(&m.q, q, 3, dims, strides, box, kv_fp8(p) ? MapType::kF16 : MapType::kBf16))
-            return s;
+        if (cpa_status s = encode(&m.q, q, 3, dims, strides, box)) return s;
     }
     const cuuint32_t box_rows = (cuuint32_t)(bs < (cuuint64_t)kTcTileN ? bs : (cuuint64_t)kTcTileN);
     if (kv_fp8(p)) {
@@ -460,12 +466,12 @@ cpa_status make_tc_maps(const cpa_batch *b, const cpa_params *p, const void *q, 
         const cuuint64_t dims3[3] = {D, Hkv, T};
         const cuuint64_t strides3[2] = {D, Hkv * D};
         const cuuint32_t box3[3] = {(cuuint32_t)D, 1, (cuuint32_t)kTcTileN};
-        if (cpa_status s = encode(&m.k_new, k_new, 3, dims3, strides3, box3, MapType::kCodes)) return s;
+        if (cpa_status s = encode(&m.k_new, k_new, 3, dims3, strides3, box3, MapType::kCodesMma)) return s;
         if (cpa_status s = encode(&m.v_new, v_new, 3, dims3, strides3, box3, MapType::kCodes)) return s;
         const cuuint64_t dims4[4] = {D, Hkv, bs, (cuuint64_t)p->num_blocks};
         const cuuint64_t strides4[3] = {D, Hkv * D, bs * Hkv * D};
         const cuuint32_t box4[4] = {(cuuint32_t)D, 1, box_rows, 1};
-        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims4, strides4, box4, MapType::kCodes)) return s;
+        if (cpa_status s = encode(&m.k_pool, k_cache, 4, dims4, strides4, box4, MapType::kCodesMma)) return s;
         return encode(&m.v_pool, v_cache, 4, dims4, strides4, box4, MapType::kCodes);
     }
     {
@@ -617,7 +623,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         r.k_rot = (r.rotate && !r.kv_fp8) ? ws + pl.rk_off : nullptr;
         r.k_q8 = r.kv_fp8 ? ws + pl.kq_off : nullptr;
         r.v_q8 = r.kv_fp8 ? ws + pl.vq_off : nullptr;
-        r.q16 = r.kv_fp8 ? ws + pl.q16_off : nullptr;
+        r.q8 = r.kv_fp8 ? ws + pl.q8_off : nullptr;
         r.q_rscale = r.kv_fp8 ? reinterpret_cast<float *>(ws + pl.qs_off) : nullptr;
         r.write_pool = fuse_write ? 1 : 0;
         r.k_cache = k_cache;
@@ -625,7 +631,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         if (r.q_rot) q = r.q_rot;
         if (r.k_rot) k_new = r.k_rot;
         if (r.kv_fp8) {
-            q = r.q16;
+            q = r.q8;
             k_new = r.k_q8;
             v_new = r.v_q8;
             q_rscale = r.q_rscale;

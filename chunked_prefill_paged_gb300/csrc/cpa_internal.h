@@ -159,7 +159,8 @@ struct AttnArgs {
     int test_stall;     // testing only: withhold the first K tile's copies
     // FP8 cache: pools and k_new / v_new (the workspace copies of the new rows'
     // codes) hold E4M3 codes; a code of kv head g stands for value * scale[g].
-    // q is then fp16, row (t, h) scaled by 2^e; q_rscale[t * hq + h] = 2^-e.
+    // q is then two E4M3 planes [2][T, hq, d] (a row scaled by 2^e, and its
+    // rounding residual); q_rscale[t * hq + h] = 2^-e.
     int kv_fp8;
     const float *k_scale;  // [hkv]
     const float *v_scale;  // [hkv]
@@ -224,8 +225,8 @@ struct RopeArgs {
     const float *v_scale; // [hkv]
     void *k_q8;           // [T, hkv, d] codes of the keys, or null
     void *v_q8;           // [T, hkv, d] codes of the values, or null
-    void *q16;            // [T, hq, d] fp16 queries (FP8-cache attention), or null
-    float *q_rscale;      // [T, hq] inverse power-of-two scale of each q16 row
+    void *q8;             // [2][T, hq, d] E4M3 planes of the scaled queries (FP8-cache attention), or null
+    float *q_rscale;      // [T, hq] inverse power-of-two scale of each q8 row
 };
 
 // Arguments of the standalone KV write.

@@ -54,11 +54,13 @@ cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stre
 // element x of kv head g becomes the E4M3 code of fl32(x / scale[g]) --
 // correctly rounded division, then the hardware conversion, round to
 // nearest even with saturation to +-448.  The attention over FP8 pools runs
-// its MMAs in fp16, so each query row (after rotation, as the element type)
-// is also written as fp16 times 2^e, e chosen so that the row's largest
-// magnitude lands in [2^14, 2^15): every element within 2^-28 of that
-// maximum converts exactly (bf16 keeps 8 significant bits, fp16 11), and
-// 2^-e goes to q_rscale for the softmax to undo.
+// its score MMAs on E4M3 operands, so each query row (after rotation, as the
+// element type) is scaled by 2^e, e chosen so that the row's largest
+// magnitude lands in [2^7, 2^8) (below the E4M3 maximum 448), and written as
+// two E4M3 planes: a = E4M3(y) and b = E4M3(y - a), y the scaled element
+// (y - a is exact in fp32).  a + b is within 2^-8 |y| of y (plus 2^-10 near
+// the bottom of the range, 2^-18 of the row's maximum), about the precision
+// of bf16; 2^-e goes to q_rscale for the softmax to undo.
 //
 // Lane l owns pairs c = 2l, 2l + 1 (d = 128) or c = l (d = 64), so the warp's
 // accesses to each half row are contiguous.
@@ -73,6 +75,14 @@ template <> struct LaneVec<8> { using type = uint2; };
 
 __device__ __forceinline__ uint8_t e4m3_code(float x, float scale) {
     return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+}
+
+// y as two E4M3 codes: a = E4M3(y), b = E4M3(y - value(a)) (nearest even,
+// saturating; y - value(a) is exact in fp32)
+__device__ __forceinline__ void e4m3_split(float y, uint8_t &a, uint8_t &b) {
+    a = (uint8_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+    const float va = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)a, __NV_E4M3)));
+    b = (uint8_t)__nv_cvt_float_to_fp8(y - va, __NV_SATFINITE, __NV_E4M3);
 }
 
 // the PPL codes of a lane's elements, packed as they lie in memory
@@ -95,7 +105,7 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     for (int c = threadIdx.x; c < HALF; c += blockDim.x) frac_s[c] = a.turn_frac[c];
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int head_lo = (a.q_rot || a.q16) ? 0 : a.hq;  // key heads only unless queries are written
+    const int head_lo = (a.q_rot || a.q8) ? 0 : a.hq;  // key heads only unless queries are written
     const int heads = a.hq + a.hkv;
     const int groups = (heads - head_lo + kHeadsPerWarp - 1) / kHeadsPerWarp;
     const long long wid = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -155,8 +165,8 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
                 xh.e[e] = from_float<T>(y1);
             }
         }
-        if (is_q && a.q16) {
-            // fp16 copy scaled by 2^e per row (see above)
+        if (is_q && a.q8) {
+            // two E4M3 planes of the row scaled by 2^e (see above)
             float amax = 0.f;
 #pragma unroll
             for (int e = 0; e < PPL; ++e) amax = fmaxf(amax, fmaxf(fabsf(to_float(xl.e[e])), fabsf(to_float(xh.e[e]))));
@@ -164,20 +174,23 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             int ex = 0;
             if (amax > 0.f) frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-            const int e = max(-100, min(100, amax > 0.f ? 15 - ex : 0));
+            const int e = max(-100, min(100, amax > 0.f ? 8 - ex : 0));
             const float up = __int_as_float((127 + e) << 23), down = __int_as_float((127 - e) << 23);
-            union {
-                typename LaneVec<PPL * 2>::type v;
-                __half e[PPL];
-            } q_lo, q_hi;
+            union Codes {
+                C8 v;
+                uint8_t b[PPL];
+            } pa_lo, pa_hi, pb_lo, pb_hi;
 #pragma unroll
             for (int e2 = 0; e2 < PPL; ++e2) {
-                q_lo.e[e2] = __float2half_rn(to_float(xl.e[e2]) * up);
-                q_hi.e[e2] = __float2half_rn(to_float(xh.e[e2]) * up);
+                e4m3_split(to_float(xl.e[e2]) * up, pa_lo.b[e2], pb_lo.b[e2]);
+                e4m3_split(to_float(xh.e[e2]) * up, pa_hi.b[e2], pb_hi.b[e2]);
             }
-            __half *dst = static_cast<__half *>(a.q16) + row;
-            *reinterpret_cast<typename LaneVec<PPL * 2>::type *>(dst + lane * PPL) = q_lo.v;
-            *reinterpret_cast<typename LaneVec<PPL * 2>::type *>(dst + HALF + lane * PPL) = q_hi.v;
+            uint8_t *dst = static_cast<uint8_t *>(a.q8) + row;
+            const long long plane = (long long)a.total_tokens * a.hq * D;
+            *reinterpret_cast<C8 *>(dst + lane * PPL) = pa_lo.v;
+            *reinterpret_cast<C8 *>(dst + HALF + lane * PPL) = pa_hi.v;
+            *reinterpret_cast<C8 *>(dst + plane + lane * PPL) = pb_lo.v;
+            *reinterpret_cast<C8 *>(dst + plane + HALF + lane * PPL) = pb_hi.v;
             if (lane == 0) a.q_rscale[(long long)t * a.hq + hh] = down;
             continue;
         }
@@ -228,7 +241,7 @@ cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (a.total_tokens == 0) return cudaSuccess;
     const int warps = 8;
-    const int heads = (a.q_rot || a.q16) ? a.hq + a.hkv : a.hkv;
+    const int heads = (a.q_rot || a.q8) ? a.hq + a.hkv : a.hkv;
     const long long work = (long long)a.total_tokens * ((heads + kHeadsPerWarp - 1) / kHeadsPerWarp);
     const int blocks = (int)((work + warps - 1) / warps);
     if (a.elem_bytes == 2) {

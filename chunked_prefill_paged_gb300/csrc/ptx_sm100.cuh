@@ -308,6 +308,39 @@ __device__ __forceinline__ void umma_s_tile128(uint32_t d_tmem, uint32_t a_lo, u
         : "memory");
 }
 
+// One score tile S = (Qa + Qb) K^T at head_dim 128 with E4M3 operands: the
+// queries as two E4M3 planes (a row and its rounding residual), each a
+// K-major 128-byte-swizzled tile of 128 one-byte columns, and K one such
+// tile of codes.  Four .kind::f8f6f4 MMAs per plane (K steps of 32 elements
+// = 32 bytes = 2 units), the eight under one elect.sync; plane b starts
+// plane_units after plane a.  The first MMA overwrites D.
+__device__ __forceinline__ void umma_s_tile_e4m3(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
+                                                 uint32_t idesc, uint32_t plane_units) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 a, b;\n\t.reg .b64 ad, bd;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "mov.b64 ad, {%1, %3};\n\tmov.b64 bd, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pf;\n\t"
+        "add.u32 a, %1, 2;\n\tadd.u32 b, %2, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, 4;\n\tadd.u32 b, %2, 4;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, 6;\n\tadd.u32 b, %2, 6;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, %1, %5;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, %2, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, b, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t"
+        "add.u32 a, a, 2;\n\tadd.u32 b, b, 2;\n\tmov.b64 ad, {a, %3};\n\tmov.b64 bd, {b, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, pt;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(plane_units)
+        : "memory");
+}
+
 // One PV product over a 128-key tile: O (+)= P V with P read from TMEM
 // (16 keys = 8 columns of bf16 pairs per MMA) and V an MN-major tile (16 key
 // rows = 2048 bytes = 128 units per MMA); eight MMAs under one elect.sync.
@@ -461,6 +494,14 @@ __host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N, int a_mn, i
 
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
     return idesc_16bit_f32(M, N, a_mn, b_mn, true);
+}
+
+// Instruction descriptor, .kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), both K-major, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                      // D format: f32
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
 }  // namespace ptx
