@@ -51,10 +51,12 @@
  *     active tokens' own new rows included -- through this encoding, so a
  *     prompt prefilled in chunks over the FP8 cache gives the same result as
  *     in one call (a NaN code inside a request's visible keys gives an
- *     unspecified result).  The attention then multiplies in fp16: each query
+ *     unspecified result).  The scores multiply E4M3 operands: each query
  *     row is scaled by a power of two that puts its largest magnitude in
- *     [2^14, 2^15) (exact for every element within 2^-28 of that maximum)
- *     and the probabilities are rounded to fp16 (finer than bf16).
+ *     [2^7, 2^8) and taken as two E4M3 terms, a = E4M3(y) and b = E4M3(y - a)
+ *     (within 2^-8 |y| of y, about bf16 precision), against the key codes;
+ *     the values multiply in fp16 (every E4M3 value is an fp16 value) with
+ *     the probabilities rounded to fp16.
  *     ("Prefill Optimisation", section 3, prefix caching: the KV cache data
  *     type, e.g. FP8 E4M3, and its quantization scales are part of what the
  *     cached KV means; the pages fix nothing further, so the format and this
@@ -163,7 +165,10 @@ typedef struct {
                                  (x_c, x_{c+d/2}) turned by p * rope_theta^(-2c/d) (rotate-half
                                  form), in fp32 and rounded to the element type.  The rotated keys
                                  are what the K/V write stores.  The caller's q and k_new are not
-                                 modified: the rotated copies live in the workspace. */
+                                 modified: the rotated keys live in the workspace (the
+                                 tensor-core kernel with plain pools rotates the queries in
+                                 shared memory in the same launch; the CUDA-core kernel and FP8
+                                 pools take rotated query copies from a pre-pass). */
     int32_t kv_format;        /* cpa_kv_format; CPA_KV_SAME for plain pools */
     const float *k_scale;     /* CPA_KV_FP8_E4M3 only: device [H_kv], finite and > 0 (the caller's
                                  guarantee; 4-byte aligned, else CPA_ERR_INVALID_ARG); NULL otherwise */
@@ -177,14 +182,16 @@ typedef struct {
  *     The plan depends on the device's SM count: how many of the last
  *     requests take the shorter pieces of the split plan's last wave, and
  *     the tail cut.  With no device present there is neither;
- *   - the rotated copies of q and k_new when rope_theta > 0 (plain pools);
- *   - with the FP8 cache: the fp16 copy of q ([T, H_q, d] x 2 bytes), its row
- *     scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new
+ *   - when rope_theta > 0 (plain pools): the rotated copy of k_new, and on
+ *     the CUDA-core kernel of q too;
+ *   - with the FP8 cache: the two E4M3 planes of q ([2][T, H_q, d] bytes),
+ *     its row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new
  *     ([T, H_kv, d] bytes each);
  *   - when the batch runs on the tensor-core kernel (BF16 with num_heads_q /
- *     num_heads_kv dividing 128): that persistent kernel's work counter and
- *     one counter per softmax warp of every tail-cut tile (4 bytes each,
- *     rounded up to 256 bytes).
+ *     num_heads_kv dividing 128): that persistent kernel's work counter, one
+ *     counter per softmax warp of every tail-cut tile, and with rope_theta >
+ *     0 (plain pools) the key rotation's 2 + ceil(T / 128) counters (4 bytes
+ *     each, rounded up to 256 bytes).
  * 0 for an empty batch and for a CUDA-core batch with no split.  Reads only
  * host mirrors.  Returns 0 also when the arguments are invalid;
  * chunked_prefill_attention then reports the error. */
