@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                                                           : mbar_try_wait(&sh.q_empty[qb], par)))
                             return false;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qb], TB);
+                    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qb], (uint32_t)(a.tile_m * D * 2));  // tile_m rows
                     __syncwarp();
                     const int tok0 = uq.cu0 + uq.row0 / a.G;
                     if (F8) {

@@ -119,12 +119,18 @@ bool use_tensor_cores(const cpa_params *p) {
     if (p->dtype != CPA_DTYPE_BF16) return false;
     if (p->flags & CPA_FLAG_FORCE_SIMT) return false;
     const int G = p->num_heads_q / p->num_heads_kv;
-    // a query tile is one TMA box of (64, G, 128 / G): G must divide 128
-    return G <= kTcTileM && (kTcTileM % G) == 0;
+    return G <= kTcTileM;
 }
+
+// Packed query rows of a tensor-core tile: the whole tokens that fit 128 MMA
+// rows (a query tile is one TMA box of (d, G, 128 / G) -- G query heads of
+// floor(128 / G) tokens), so that no token's rows straddle two tiles; the
+// MMA rows past it (128 mod G of them) carry nothing that reaches an output.
+int tc_tile_m(int G) { return G * (kTcTileM / G); }
 
 struct Plan {
     int tile_m = 0;
+    bool tc = false;         // the tensor-core kernels (else the CUDA-core one)
     bool tc2 = false;        // the two-pipeline tensor-core kernel (attn_tc2.cu)
     bool rope_fused = false; // the one-pipeline kernel rotates queries and keys itself
     int tiles_per_unit = 1;
@@ -310,22 +316,25 @@ size_t counter_ints(const cpa_batch *b, const Plan &pl) {
 Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     Plan pl;
     const bool tc = use_tensor_cores(p);
-    pl.tile_m = tc ? kTcTileM : kSimtTileM;
+    const int G = p->num_heads_q / p->num_heads_kv;
+    pl.tc = tc;
+    pl.tile_m = tc ? tc_tile_m(G) : kSimtTileM;
     // The two-pipeline kernel (attn_tc2.cu) runs BF16 batches at block sizes
     // 16 and 32 that have query tiles to pair: a 128-key tile there takes 16
     // or 8 TMA boxes per operand, and pairs halve the boxes per FLOP.  The
     // one-pipeline kernel (attn_tc.cu) runs the rest -- block sizes 64 and
     // 128, decode-only batches (both measured faster on it), FP8 pools and
     // the opt-in tail cut, and the rotary embedding (which it applies in the
-    // same launch).  Pairs unless a batch of direct units only schedules
-    // better with single tiles (choose_tiles_per_unit, below).
-    const int G = p->num_heads_q / p->num_heads_kv;
+    // same launch), and query groups that do not divide 128.  Pairs unless a
+    // batch of direct units only schedules better with single tiles
+    // (choose_tiles_per_unit, below).
     bool pairs = false;
     for (int r = 0; r < b->num_reqs && !pairs; ++r)
         pairs = (long long)b->h_num_new_tokens[r] * G > kTcTileM;
     const bool rope = p->rope_theta > 0.f;
     pl.rope_fused = tc && !kv_fp8(p) && rope;
-    pl.tc2 = tc && !kv_fp8(p) && !rope && !(p->flags & CPA_FLAG_TAIL_SPLIT) && p->block_size <= 32 && pairs;
+    pl.tc2 = tc && (kTcTileM % G) == 0 && !kv_fp8(p) && !rope && !(p->flags & CPA_FLAG_TAIL_SPLIT) &&
+             p->block_size <= 32 && pairs;
     pl.tiles_per_unit = pl.tc2 ? 2 : 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     // fewer, longer split units while the batch keeps enough of them: every
@@ -660,7 +669,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.tile_m = pl.tile_m;
     a.tiles_per_unit = pl.tiles_per_unit;
     a.head_major = pl.head_major;
-    a.interleave = (pl.tile_m == kTcTileM && pl.direct_units > 0 && pl.split_units > 0) ? 1 : 0;
+    a.interleave = (pl.tc && pl.direct_units > 0 && pl.split_units > 0) ? 1 : 0;
     a.interleave_span = pl.direct_units + pl.split_units - pl.fine_units;
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
@@ -676,7 +685,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.lse = lse;
     a.ws = static_cast<float *>(workspace);
     a.fuse_write = fuse_write ? 1 : 0;
-    if (pl.tile_m == kTcTileM && fuse_write) {
+    if (pl.tc && fuse_write) {
         const long long pieces = (long long)batch->total_new_tokens * params->num_heads_kv *
                                  (params->head_dim * elem_bytes(params) / 16);
         a.write_chunks = (int)((pieces + kWriteChunkPieces - 1) / kWriteChunkPieces);
@@ -685,7 +694,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     // the tensor-core kernel is persistent: at most one CTA per SM, and no
     // more than it has attention units and write pieces
     const int work = units + a.write_chunks;
-    a.write_ctas = (pl.tile_m == kTcTileM) ? (work < dev.sms ? work : dev.sms) : units;
+    a.write_ctas = pl.tc ? (work < dev.sms ? work : dev.sms) : units;
     a.err = dev.err;
     a.timeout_cycles = params->timeout_cycles > 0 ? params->timeout_cycles : kDefaultTimeoutCycles;
     a.test_stall = (params->flags & CPA_FLAG_TEST_STALL) ? 1 : 0;
@@ -706,7 +715,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     }
 
     cudaError_t e;
-    if (pl.tile_m == kTcTileM) {
+    if (pl.tc) {
         TcMaps maps;
         if (cpa_status s = make_tc_maps(batch, params, q, k_new, v_new, k_cache, v_cache, maps)) return s;
         if (prepass && launch_rope(r, dev.sms, st) != cudaSuccess) return CPA_ERR_CUDA;

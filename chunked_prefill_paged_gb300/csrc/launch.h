@@ -11,7 +11,7 @@ namespace cpa {
 
 // Tensor maps for the tensor-core kernel (see attn_tc.cu).
 struct TcMaps {
-    CUtensorMap q;       // q      [T, H_q, d]   box (64, G, 128/G)
+    CUtensorMap q;       // q      [T, H_q, d]   box (64, G, floor(128/G))
     CUtensorMap k_new;   // k_new  [T, H_kv, d]  box (64, 1, 128)
     CUtensorMap v_new;
     CUtensorMap k_pool;  // pool   [blocks, bs, H_kv, d]  box (64, 1, bs, 1)

@@ -102,7 +102,7 @@ typedef enum {
     CPA_KV_SAME = 0,      /* the pools hold elements of cpa_params.dtype */
     CPA_KV_FP8_E4M3 = 1   /* the pools hold FP8 E4M3 codes with per-kv-head scales (BF16
                              dtype; chunked_prefill_attention also needs head_dim 128 and
-                             num_heads_q / num_heads_kv dividing 128, else CPA_ERR_UNSUPPORTED) */
+                             num_heads_q / num_heads_kv at most 128, else CPA_ERR_UNSUPPORTED) */
 } cpa_kv_format;
 
 /* flags (cpa_params.flags) */
@@ -188,7 +188,7 @@ typedef struct {
  *     its row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new
  *     ([T, H_kv, d] bytes each);
  *   - when the batch runs on the tensor-core kernel (BF16 with num_heads_q /
- *     num_heads_kv dividing 128): that persistent kernel's work counter, one
+ *     num_heads_kv at most 128): that persistent kernel's work counter, one
  *     counter per softmax warp of every tail-cut tile, and with rope_theta >
  *     0 (plain pools) the key rotation's 2 + ceil(T / 128) counters (4 bytes
  *     each, rounded up to 256 bytes).

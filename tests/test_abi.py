@@ -195,16 +195,23 @@ def test_fp8_arguments_checked_before_launch(lib, case, expect):
     assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == 0
 
 
-@pytest.mark.parametrize("kw", [dict(head_dim=64), dict(num_heads_q=24), dict(flags=0x2)])
+@pytest.mark.parametrize("kw", [dict(head_dim=64), dict(flags=0x2)])
 def test_fp8_attention_needs_the_tensor_core_kernel(lib, kw):
-    # d = 64, a query group that does not divide 128 (G = 3), or a forced
-    # CUDA-core kernel: the FP8 cache runs on the tensor-core kernel only
+    # d = 64 or a forced CUDA-core kernel: the FP8 cache runs on the
+    # tensor-core kernel only (a query group that does not divide 128, G = 3,
+    # runs there too: 126-row query tiles)
     p = _fp8_params(lib, **kw)
     b, keep = _cbatch(lib, [10], [5], 4)
     L = lib.load()
     assert L.chunked_prefill_attention(ctypes.byref(b), ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, 0,
                                        None) == lib.ERR_UNSUPPORTED
     assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == 0
+
+
+def test_fp8_attention_takes_query_groups_that_do_not_divide_128(lib):
+    p = _fp8_params(lib, num_heads_q=24)  # G = 3
+    b, keep = _cbatch(lib, [10], [5], 4)
+    assert lib.load().chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) > 0
 
 
 def test_workspace_size_counts_fp8_codes(lib):

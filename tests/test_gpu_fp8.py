@@ -262,11 +262,11 @@ def test_every_code_scores_exactly_through_the_key_path(cpa):
             assert np.all(err <= 2e-6 * np.maximum(1.0, np.abs(want))), (name, codes, got, want)
 
 
-@pytest.mark.parametrize("bs,hq", [(32, 16), (64, 64)])
-def test_fp8_other_block_sizes_and_groups(cpa, bs, hq):
-    # block sizes 32 / 64 (several code boxes per key tile) and G = 8 query
-    # heads per kv head (the long-context shape)
-    w = W.make_batch_workload(f"fp8_b{bs}", W.Shape(hq, 8 if hq == 64 else 4, 128, bs, 1024, "bf16"),
+@pytest.mark.parametrize("bs,hq,hkv", [(32, 16, 4), (64, 64, 8), (16, 28, 4)])
+def test_fp8_other_block_sizes_and_groups(cpa, bs, hq, hkv):
+    # block sizes 32 / 64 (several code boxes per key tile), G = 8 query heads
+    # per kv head (the long-context shape) and G = 7 (126-row query tiles)
+    w = W.make_batch_workload(f"fp8_b{bs}_{hq}", W.Shape(hq, hkv, 128, bs, 1024, "bf16"),
                               [(0, 150), (2000, 1), (513, 64), (4096, 1)], seed=67)
     res = run_fp8(cpa, w)
     assert_within(res, "bf16")

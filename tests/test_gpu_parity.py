@@ -68,6 +68,26 @@ def test_small_batch_tensor_cores(cpa, hq, hkv, d, bs, variant):
     assert_within(res, "bf16")
 
 
+# query groups that do not divide 128 run on the tensor cores with query tiles
+# of G * floor(128 / G) rows (126, 125, 120): a token's rows never straddle
+# two tiles, and the MMA rows past them carry nothing to an output
+@pytest.mark.parametrize("hq,hkv,d,bs", [(6, 2, 128, 16), (28, 4, 128, 16), (12, 2, 64, 128), (20, 4, 128, 32),
+                                         (24, 2, 128, 16)])
+@pytest.mark.parametrize("variant", W.VARIANTS)
+def test_small_batch_tensor_cores_uneven_groups(cpa, hq, hkv, d, bs, variant):
+    w = small_batch(hq, hkv, d, bs)
+    res = run_and_compare(w, variant=variant)
+    assert_within(res, "bf16")
+
+
+def test_uneven_group_with_the_tail_cut_and_no_split(cpa):
+    w = small_batch(28, 4, 128, 16, reqs=[(3000, 900), (0, 700), (5000, 1), (70, 3)], seed=9)
+    res = run_and_compare(w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_TAIL_SPLIT)
+    assert_within(res, "bf16")
+    res = run_and_compare(w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_NO_SPLIT, variant="needle")
+    assert_within(res, "bf16")
+
+
 def test_small_batch_cuda_cores_bf16(cpa):
     w = small_batch()
     res = run_and_compare(w, flags=cpa.FLAG_FUSE_KV_WRITE | cpa.FLAG_FORCE_SIMT)

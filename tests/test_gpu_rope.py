@@ -192,7 +192,8 @@ def run_rope(cpa, w, *, flags=None, rows_per_req=None, steps_to_check=None, vari
 # (every row its own token), G = 16 and 32 (few tokens per query tile), head
 # dimension 64 (both halves of a pair in one 128-byte row); prefills with and
 # without cached keys, a ragged chunk and decodes (split units) side by side.
-@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 8, 128, 16), (16, 1, 128, 128), (8, 2, 64, 16), (64, 2, 128, 32)])
+@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 8, 128, 16), (16, 1, 128, 128), (8, 2, 64, 16), (64, 2, 128, 32),
+                                         (28, 4, 128, 16)])
 def test_rope_tensor_core_shapes(cpa, hq, hkv, d, bs):
     reqs = [(0, 300), (130, 77), (1000, 1), (257, 129), (4000, 1)]
     w = W.make_batch_workload(f"rope_tc_{hq}_{hkv}_{d}_{bs}", W.Shape(hq, hkv, d, bs, 512, "bf16"), reqs, seed=44)

@@ -255,3 +255,16 @@ def test_bench_kernel_labels_follow_the_planner(harness):
         got_rope = plan(harness, reqs, hq=sh.num_heads_q, hkv=sh.num_heads_kv, d=sh.head_dim, bs=sh.block_size,
                         seg=sh.kv_segment_size, rope=500000.0)
         assert bench.tc_kernel_name(sh, s, rope=True).startswith("attn_tc2_kernel") == bool(got_rope["tc2"])
+
+
+@pytest.mark.parametrize("hq,hkv,want", [(32, 8, 128), (24, 8, 126), (28, 4, 126), (24, 4, 126), (20, 4, 125),
+                                         (96, 8, 120), (128, 1, 128), (100, 1, 100)])
+def test_query_tiles_hold_whole_tokens(harness, hq, hkv, want):
+    # a tensor-core query tile is G * floor(128 / G) packed rows: whole tokens
+    # only, for every query group up to 128; the two-pipeline kernel (which
+    # pairs 128-row tiles) takes only groups that divide 128
+    G = hq // hkv
+    got = plan(harness, [(4096, 700), (100, 1)], hq=hq, hkv=hkv)
+    assert got["tile_m"] == want == G * (128 // G)
+    if 128 % G:
+        assert got["tc2"] == 0
