@@ -64,6 +64,8 @@ CASES = {
     "long_context_last": (W.long_context, -1, 0.0, False),
     "mixed_step": (W.mixed_step, 0, 0.0, False),
     "prefix_cache": (W.prefix_cache, 0, 0.0, False),
+    "prefix_cache_rope": (W.prefix_cache, 0, 500000.0, False),
+    "long_context_last_rope": (W.long_context, -1, 500000.0, False),
     "speculative_decode": (W.speculative_decode, 0, 0.0, False),
     "llama_chunk_fp8": (W.llama3_8b_prompt, -1, 0.0, True),
     "mixed_step_fp8": (W.mixed_step, 0, 0.0, True),
@@ -462,10 +464,11 @@ def warm_cache(cpa, w, t, params, dev, upto):
 def tc_kernel_name(sh, step, rope=False, fp8=False):
     """The tensor-core kernel the library's planner picks for this batch (its
     rule, restated for labelling): the two-pipeline kernel for BF16 pools at
-    block sizes up to 32 with query tiles to pair and no rotary embedding."""
+    block sizes up to 32 with query tiles to pair and a query group dividing
+    128 (with the rotary embedding after the rotation pre-pass)."""
     G = sh.num_heads_q // sh.num_heads_kv
     pairs = any(int(n) * G > 128 for n in step.num_new_tokens)
-    if not fp8 and not rope and sh.block_size <= 32 and pairs:
+    if not fp8 and 128 % G == 0 and sh.block_size <= 32 and pairs:
         return f"attn_tc2_kernel<{sh.head_dim}>"
     return f"attn_tc_kernel<{sh.head_dim}, {'true' if fp8 else 'false'}>"
 

@@ -324,17 +324,18 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
     // or 8 TMA boxes per operand, and pairs halve the boxes per FLOP.  The
     // one-pipeline kernel (attn_tc.cu) runs the rest -- block sizes 64 and
     // 128, decode-only batches (both measured faster on it), FP8 pools and
-    // the opt-in tail cut, and the rotary embedding (which it applies in the
-    // same launch), and query groups that do not divide 128.  Pairs unless a
-    // batch of direct units only schedules better with single tiles
+    // the opt-in tail cut, and query groups that do not divide 128.  Pairs
+    // unless a batch of direct units only schedules better with single tiles
     // (choose_tiles_per_unit, below).
     bool pairs = false;
     for (int r = 0; r < b->num_reqs && !pairs; ++r)
         pairs = (long long)b->h_num_new_tokens[r] * G > kTcTileM;
     const bool rope = p->rope_theta > 0.f;
-    pl.rope_fused = tc && !kv_fp8(p) && rope;
-    pl.tc2 = tc && (kTcTileM % G) == 0 && !kv_fp8(p) && !rope && !(p->flags & CPA_FLAG_TAIL_SPLIT) &&
-             p->block_size <= 32 && pairs;
+    pl.tc2 = tc && (kTcTileM % G) == 0 && !kv_fp8(p) && !(p->flags & CPA_FLAG_TAIL_SPLIT) && p->block_size <= 32 &&
+             pairs;
+    // the one-pipeline kernel applies the rotary embedding in the same launch;
+    // the two-pipeline kernel reads rotated copies from the pre-pass
+    pl.rope_fused = tc && !kv_fp8(p) && rope && !pl.tc2;
     pl.tiles_per_unit = pl.tc2 ? 2 : 1;
     pl.split_len = (p->flags & CPA_FLAG_NO_SPLIT) ? 0 : (p->kv_segment_size > 0 ? p->kv_segment_size : kDefaultSplit);
     // fewer, longer split units while the batch keeps enough of them: every

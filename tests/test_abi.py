@@ -150,14 +150,22 @@ def test_workspace_size_counts_split_partials(lib):
 def test_workspace_size_counts_rotated_copies(lib):
     L = lib.load()
     b, keep = _cbatch(lib, [8000], [512], 600)
-    plain = L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(lib.Params(32, 8, 128, 16, 10000, 1024).c()))
-    p = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0).c()
     rq = 512 * 32 * 128 * 2   # rotated queries, bf16
     rk = 512 * 8 * 128 * 2    # rotated new keys
-    # tensor-core kernel: the queries are rotated in shared memory, so only the
-    # keys' copy comes first (256-byte aligned); the counters stay last (the
-    # work counter and the rotation's 2 + 4 counts fit the same 256 bytes)
-    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rk + plain
+    # block size 128, the one-pipeline kernel: the queries are rotated in
+    # shared memory, so only the keys' copy comes first (256-byte aligned); the
+    # counters stay last (the work counter and the rotation's 2 + 4 counts fit
+    # the same 256 bytes)
+    b128, keep128 = _cbatch(lib, [8064], [512], 80)
+    plain = L.chunked_prefill_workspace_size(ctypes.byref(b128),
+                                             ctypes.byref(lib.Params(32, 8, 128, 128, 1000, 1024).c()))
+    p = lib.Params(32, 8, 128, 128, 1000, 1024, rope_theta=500000.0).c()
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b128), ctypes.byref(p)) == rk + plain
+    # block size 16 with query tiles to pair, the two-pipeline kernel: the
+    # rotation pre-pass writes copies of both
+    plain = L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(lib.Params(32, 8, 128, 16, 10000, 1024).c()))
+    p = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0).c()
+    assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(p)) == rq + rk + plain
     # the CUDA-core kernel (forced) reads rotated copies of both, and keeps no counter
     ps = lib.Params(32, 8, 128, 16, 10000, 1024, rope_theta=500000.0, flags=lib.FLAG_FORCE_SIMT).c()
     assert L.chunked_prefill_workspace_size(ctypes.byref(b), ctypes.byref(ps)) == rq + rk

@@ -230,10 +230,11 @@ def test_kernel_choice(harness):
     assert plan(harness, [(8192, 1)] * 8, bs=16)["tc2"] == 0
     assert plan(harness, [(30720, 2048)], bs=16, kv_format=1)["tc2"] == 0
     assert plan(harness, [(30720, 2048)], bs=16, flags=FUSE | TAIL_SPLIT)["tc2"] == 0
-    # the rotary embedding: the one-pipeline kernel, which applies it in the
-    # same launch (BF16 pools); FP8 pools keep the pre-pass
+    # the rotary embedding: the one-pipeline kernel applies it in the same
+    # launch (BF16 pools); the two-pipeline kernel and FP8 pools take the
+    # rotation pre-pass
     got = plan(harness, [(30720, 2048)], bs=16, rope=500000.0)
-    assert (got["tc2"], got["rope_fused"], got["tiles_per_unit"]) == (0, 1, 1)
+    assert (got["tc2"], got["rope_fused"]) == (1, 0)
     assert plan(harness, [(8192, 1808)], bs=128, rope=500000.0)["rope_fused"] == 1
     assert plan(harness, [(8192, 1808)], bs=128, kv_format=1, rope=500000.0)["rope_fused"] == 0
     assert plan(harness, [(8192, 1808)], bs=128)["rope_fused"] == 0
