@@ -20,11 +20,7 @@
 //              row: warp w covers TMEM lanes 32 (w % 4) + 16 (w / 4) .. +15,
 //              its threads 0-15 the row's keys 0-63 (output columns 0 .. D/2-1)
 //              and threads 16-31 keys 64-127 (columns D/2 .. D-1); the row
-//              maximum and sum are combined with one shuffle.  They also do
-//              the fused K/V write: its pieces follow the attention units in
-//              the work counter, so CTAs whose attention work has run out take
-//              them (this kernel reads new keys from k_new / v_new, so the
-//              pool rows are only needed by the next call).
+//              maximum and sum are combined with one shuffle.
 //              With the rotary embedding they first rotate the launch's new
 //              keys, once, from k_src into the workspace copy k_new that the
 //              new-key tiles and the fused write read: pieces of 16 tokens
@@ -47,7 +43,10 @@
 //   warps 12-15 (BF16 pools) output epilogue; with the rotary embedding they
 //              also rotate each unit's query tile in its Q stage once it has
 //              landed, one unit ahead of the outputs, and the score MMAs wait
-//              for that (q_rot) instead of the copy.
+//              for that (q_rot) instead of the copy.  They also do the fused
+//              K/V write, an even share per CTA while its first unit runs
+//              (this kernel reads new keys from k_new / v_new, so the pool
+//              rows are only needed by the next call).
 //   warps 12-15 (FP8 pools) expand E4M3 value code tiles in place into the
 //              fp16 tiles the PV MMAs read (32 rows each).  The score MMAs read
 //              the key codes as they landed (E4M3 operands, .kind::f8f6f4), with
@@ -477,7 +476,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     const int lane = tid & 31;
     const long long LIM = a.timeout_cycles;
     const int total_units = attention_units(a);
-    const int end_index = total_units + a.write_chunks;  // then the fused K/V write
+    const int end_index = total_units;  // the counter's indices past the work
 
     if (tid == 0) {
         for (int b = 0; b < Cfg::kQStages; ++b) {
@@ -579,11 +578,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                         break;
                     }
                     if (unit < total_units) decode_unit(a, unit, u);  // once, for every role
-                    if (lane == 0) {
-                        publish_unit(sh.ring, it, unit, u);
-                        // pieces of the K/V write need no copies: claim the next index now
-                        if (unit >= total_units && unit < end_index) taken = atomicAdd(a.sched, 1);
-                    }
+                    if (lane == 0) publish_unit(sh.ring, it, unit, u);
                     __syncwarp();
                 }
             } else {
@@ -594,7 +589,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 }
             }
             if (unit >= end_index) break;
-            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             TileList tl;
             tl.init(u);
@@ -743,10 +737,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                         }
                         Unit uu;
                         if (un < total_units) decode_unit(a, un, uu);
-                        if (lane == 0) {
-                            publish_unit(sh.ring, it + 1, un, uu);
-                            if (un >= total_units && un < end_index) taken = atomicAdd(a.sched, 1);
-                        }
+                        if (lane == 0) publish_unit(sh.ring, it + 1, un, uu);
                         __syncwarp();
                         early = it + 1;
                     }
@@ -818,7 +809,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 break;
             }
             if (unit >= end_index) break;
-            if (unit >= total_units) continue;  // a piece of the K/V write: the softmax warps' job
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             TileList tl;
             tl.init(u);
@@ -946,11 +936,34 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // With the rotary embedding these warps rotate each unit's queries in
         // its Q stage, one unit ahead: the next unit's as soon as its copy
         // has landed, before this unit's outputs (which wait for its last PV).
+        //
+        // They also copy this CTA's share of the fused K/V write while the
+        // first unit runs (attention reads the new rows from k_new / v_new,
+        // never from these pool rows): at once, or with the rotary embedding
+        // after the first unit's queries and once the share's keys are rotated.
         const int e = warp - kEpiWarp;
         const int lr = 32 * e + lane;
+        const bool rope = !F8 && a.rope;
+        auto write_share = [&]() -> bool {
+            const int per = cdiv(a.total_tokens, (int)gridDim.x);
+            const int t0 = (int)blockIdx.x * per;
+            const int t1 = t0 + per < a.total_tokens ? t0 + per : a.total_tokens;
+            if (t0 >= t1) return true;
+            const int row_bytes = a.hkv * D * 2;
+            if (rope) {
+                bool all = false;
+                if (!__all_sync(0xffffffffu, rope_rows_done(a, t0, t1, all, LIM, abort_flag))) return false;
+                write_token_rows<4, true>(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.bs, a.num_blocks,
+                                          row_bytes, a.k_new, a.v_new, a.k_cache, a.v_cache, t0, t1, lr, 128, a.err);
+            } else {
+                write_token_rows<4, false>(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.bs, a.num_blocks,
+                                           row_bytes, a.k_new, a.v_new, a.k_cache, a.v_cache, t0, t1, lr, 128, a.err);
+            }
+            return true;
+        };
+        if (a.write_share && !rope) write_share();
         const uint32_t tO = tmem + ((uint32_t)(32 * e) << 16) + kTmemO;
         bool ok = true;
-        const bool rope = !F8 && a.rope;
         // the queries of ring entry i (an attention unit uq), rotated in place
         auto rotate_q = [&](int i, const Unit &uq) -> bool {
             const int qb = i % Cfg::kQStages;
@@ -969,6 +982,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         Unit u;
         int unit = read_unit(sh.ring, 0, LIM, abort_flag, u, false);
         if (rope && unit >= 0 && unit < total_units && !rotate_q(0, u)) unit = -1;
+        if (a.write_share && rope && unit >= 0 && !write_share()) unit = -1;
         for (int ec = 0;; ++ec) {
             if (unit < 0) {
                 ok = false;
@@ -982,10 +996,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 if (unit_n >= 0 && unit_n < total_units && !rotate_q(ec + 1, un)) unit_n = -1;
             }
             reread_unit(sh.ring, ec, u);
-            if (unit >= total_units) {  // a piece of the K/V write: the softmax warps' job
-                unit = rope ? unit_n : read_unit(sh.ring, ec + 1, LIM, abort_flag, u, false);
-                continue;
-            }
             const uint32_t ph = (uint32_t)(ec & 1);
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&sh.epi_full, ph, LIM, abort_flag))) {
                 ok = false;
@@ -1125,7 +1135,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 break;
             }
             if (unit >= end_index) break;
-            if (unit >= total_units) continue;
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             TileList tl;
             tl.init(u);
@@ -1197,24 +1206,6 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 break;
             }
             if (unit >= end_index) break;
-            if (unit >= total_units) {
-                // a piece of the fused K/V write.  This kernel reads new keys
-                // from k_new / v_new, so the pool rows are only for the next
-                // call; CTAs take these pieces once attention work runs out.
-                // Rotated keys are read once the whole rotation is done.
-                bool rope_all = false;
-                if (!F8 && a.rope && !rope_rows_ready(a, 0, a.total_tokens, rope_all, LIM, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const long long total = (long long)a.total_tokens * a.hkv * (D * 2 / 16);
-                const long long b = (long long)(unit - total_units) * kWriteChunkPieces;
-                const long long e = b + kWriteChunkPieces < total ? b + kWriteChunkPieces : total;
-                scatter_new_kv(a.cached, a.cu, a.bt, a.num_reqs, a.max_blocks, a.hkv, a.bs, a.num_blocks, D * 2,
-                               a.k_new, a.v_new, a.k_cache, a.v_cache, b, e, tid, kSoftmaxThreads, a.err,
-                               !F8 && a.rope);
-                continue;
-            }
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;
             TileList tl;
             tl.init(u);
@@ -1465,8 +1456,11 @@ cudaError_t launch_tc(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_t
 }  // namespace
 
 cudaError_t launch_attn_tc(const AttnArgs &a, const TcMaps &m, cudaStream_t stream) {
-    const int grid = a.write_ctas;  // persistent: min(units + write pieces, SMs)
+    const int grid = a.write_ctas;  // persistent: min(units, SMs)
     if (grid <= 0 || attention_units(a) == 0) return cudaSuccess;
+    // the fused write is the epilogue warps' share (BF16 pools), never
+    // pieces of the work counter
+    if (a.write_chunks != 0 || (a.write_share && a.kv_fp8)) return cudaErrorInvalidValue;
     if (a.kv_fp8) return a.d == 128 ? launch_tc<128, true>(a, m, grid, stream) : cudaErrorInvalidValue;
     return a.d == 128 ? launch_tc<128, false>(a, m, grid, stream) : launch_tc<64, false>(a, m, grid, stream);
 }

@@ -687,9 +687,15 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.ws = static_cast<float *>(workspace);
     a.fuse_write = fuse_write ? 1 : 0;
     if (pl.tc && fuse_write) {
-        const long long pieces = (long long)batch->total_new_tokens * params->num_heads_kv *
-                                 (params->head_dim * elem_bytes(params) / 16);
-        a.write_chunks = (int)((pieces + kWriteChunkPieces - 1) / kWriteChunkPieces);
+        if (!pl.tc2) {
+            // the one-pipeline kernel's epilogue warps copy it while the
+            // first units run
+            a.write_share = 1;
+        } else {
+            const long long pieces = (long long)batch->total_new_tokens * params->num_heads_kv *
+                                     (params->head_dim * elem_bytes(params) / 16);
+            a.write_chunks = (int)((pieces + kWriteChunkPieces - 1) / kWriteChunkPieces);
+        }
     }
     const int units = attention_units(a);
     // the tensor-core kernel is persistent: at most one CTA per SM, and no

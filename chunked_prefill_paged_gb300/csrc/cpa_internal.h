@@ -148,10 +148,13 @@ struct AttnArgs {
     float *lse;
     float *ws;          // partials of split units
     int *sched;         // tensor-core kernel: work counter (zeroed before the launch)
-    int write_chunks;   // tensor-core kernel with the fused write: indices [units, units +
+    int write_chunks;   // two-pipeline kernel with the fused write: indices [units, units +
                         // write_chunks) of the counter are pieces of the K/V write, taken
                         // by CTAs whose attention work has run out
     int fuse_write;     // write new K/V into the pool in the same launch
+    int write_share;    // one-pipeline kernel: each CTA's epilogue warps copy an even share
+                        // of the K/V write near the start (they are idle until the first
+                        // unit ends), instead of counter pieces
     int write_ctas;     // grid size: the tensor-core kernel's persistent CTAs (units and
                         // write pieces, at most one per SM); the CUDA-core kernel's units
     int *err;           // device error word (first error wins)

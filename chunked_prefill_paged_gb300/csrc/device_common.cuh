@@ -181,7 +181,7 @@ __device__ __forceinline__ void scatter_new_kv(const int32_t *cached, const int3
                                                int num_reqs, int max_blocks, int hkv, int bs, int num_blocks,
                                                int head_bytes, const void *k_new, const void *v_new,
                                                void *k_cache, void *v_cache, long long begin, long long end,
-                                               int stride_start, int stride, int *err, bool k_written = false) {
+                                               int stride_start, int stride, int *err) {
     const int pieces_per_head = head_bytes >> 4;
     const long long per_token = (long long)hkv * pieces_per_head;
     for (long long i = begin + stride_start; i < end; i += stride) {
@@ -195,13 +195,65 @@ __device__ __forceinline__ void scatter_new_kv(const int32_t *cached, const int3
         if (slot < 0) continue;
         const long long src = ((long long)t * hkv + g) * head_bytes + p * 16;
         const long long dst = (slot * hkv + g) * head_bytes + p * 16;
-        // k_written: k_new was written earlier in this launch (the rotated
-        // keys), so it is read through the coherent path
-        const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + src);
-        const uint4 kv = k_written ? *ks : __ldg(ks);
+        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + src));
         const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(v_new) + src));
         *reinterpret_cast<uint4 *>(static_cast<char *>(k_cache) + dst) = kv;
         *reinterpret_cast<uint4 *>(static_cast<char *>(v_cache) + dst) = vv;
+    }
+}
+
+// The K and V rows of new tokens [t0, t1) into their pool slots, by
+// nthreads threads (index tid).  A token's row (all kv heads, row_bytes) is
+// contiguous both in k_new / v_new and in its slot, so a thread copies fixed
+// 16-byte columns of kBatch tokens at a time: the tokens' slots first (one
+// block-table read per token, no per-piece index arithmetic), then all loads,
+// then all stores.  kKWritten: k_new was written earlier in this launch (the
+// rotated keys) and is read through the coherent path.
+template <int kBatch, bool kKWritten>
+__device__ __forceinline__ void write_token_rows(const int32_t *cached, const int32_t *cu, const int32_t *bt,
+                                                 int num_reqs, int max_blocks, int bs, int num_blocks, int row_bytes,
+                                                 const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                                 int t0, int t1, int tid, int nthreads, int *err) {
+    if (t0 >= t1) return;
+    const int cols = row_bytes >> 4;
+    const char *kn = static_cast<const char *>(k_new);
+    const char *vn = static_cast<const char *>(v_new);
+    char *kc = static_cast<char *>(k_cache);
+    char *vc = static_cast<char *>(v_cache);
+    int r = request_of_token(cu, num_reqs, t0);
+    for (int t = t0; t < t1; t += kBatch) {
+        long long src[kBatch], dst[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int tt = t + k;
+            src[k] = 0;
+            dst[k] = -1;
+            if (tt < t1) {
+                while (r + 1 < num_reqs && __ldg(cu + r + 1) <= tt) ++r;
+                const int pos = __ldg(cached + r) + (tt - __ldg(cu + r));
+                const long long slot = slot_of(bt, max_blocks, bs, num_blocks, r, pos, err);
+                src[k] = (long long)tt * row_bytes;
+                if (slot >= 0) dst[k] = slot * row_bytes;
+            }
+        }
+        for (int c = tid; c < cols; c += nthreads) {
+            uint4 kv[kBatch], vv[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (dst[k] >= 0) {
+                    const uint4 *ks = reinterpret_cast<const uint4 *>(kn + src[k]) + c;
+                    kv[k] = kKWritten ? *ks : __ldg(ks);
+                    vv[k] = __ldg(reinterpret_cast<const uint4 *>(vn + src[k]) + c);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (dst[k] >= 0) {
+                    reinterpret_cast<uint4 *>(kc + dst[k])[c] = kv[k];
+                    reinterpret_cast<uint4 *>(vc + dst[k])[c] = vv[k];
+                }
+            }
+        }
     }
 }
 
