@@ -452,6 +452,23 @@ __device__ __forceinline__ void rope_q_tile(const AttnArgs &a, const Unit &u, ui
     }
 }
 
+// The next work index for this CTA: from its group's counter, then, once
+// that group has run out, from the other's; total_units when both have.
+__device__ __forceinline__ int claim_unit(const AttnArgs &a, int total_units) {
+    if (!a.group_ctas) return atomicAdd(a.sched, 1);
+    const bool first = (int)blockIdx.x < a.group_ctas;
+    for (int k = 0; k < 2; ++k) {
+        if (first == (k == 0)) {
+            const int i = atomicAdd(a.sched, 1);
+            if (i < a.group_units) return i;
+        } else {
+            const int i = a.group_units + atomicAdd(a.sched_b, 1);
+            if (i < total_units) return i;
+        }
+    }
+    return total_units;
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -558,7 +575,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // tile after that, with its Q copy issued then if its stage is free:
         // the next unit's first score MMA need not wait for its queries (nor,
         // with the rotary embedding, for their rotation by the epilogue warps).
-        int taken = (kv_role == 0 && lane == 0) ? atomicAdd(a.sched, 1) : 0;
+        int taken = (kv_role == 0 && lane == 0) ? claim_unit(a, total_units) : 0;
         int early = -1;        // ring entry published during the previous unit (rotary embedding)
         bool early_q = false;  // and its Q copy issued
         for (int it = 0;; ++it) {  // it: units started by this CTA
@@ -721,7 +738,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                     ok = load_kv(j, 0);
                     if (!ok || j < jc) continue;
                     if (j == jc) {
-                        if (lane == 0) taken = atomicAdd(a.sched, 1);
+                        if (lane == 0) taken = claim_unit(a, total_units);
                         continue;
                     }
                     if (early != it + 1) {
@@ -752,7 +769,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
                 }
                 // this unit's copies are all issued: claim the next unit now
                 // unless that was done above
-                if (ok && jc >= n && lane == 0) taken = atomicAdd(a.sched, 1);
+                if (ok && jc >= n && lane == 0) taken = claim_unit(a, total_units);
             } else {
                 for (int j = 0; j < n && ok; ++j) ok = load_kv(j, 1);
             }

@@ -929,7 +929,8 @@ cudaError_t launch_tc2(const AttnArgs &a, const TcMaps &m, int grid, cudaStream_
 cudaError_t launch_attn_tc2(const AttnArgs &a, const TcMaps &m, cudaStream_t stream) {
     const int grid = a.write_ctas;  // persistent: min(units + write pieces, SMs)
     if (grid <= 0 || attention_units(a) == 0) return cudaSuccess;
-    if (a.rope || a.kv_fp8) return cudaErrorNotSupported;  // the one-pipeline kernel's cases (a.rope: fused RoPE)
+    // the one-pipeline kernel's cases (a.rope: fused RoPE; two CTA groups)
+    if (a.rope || a.kv_fp8 || a.group_ctas) return cudaErrorNotSupported;
     return a.d == 128 ? launch_tc2<128>(a, m, grid, stream) : launch_tc2<64>(a, m, grid, stream);
 }
 

@@ -12,6 +12,7 @@
 #include <functional>
 #include <mutex>
 #include <queue>
+#include <utility>
 #include <vector>
 
 #include "../../include/cpa.h"
@@ -146,6 +147,8 @@ struct Plan {
     int fine_units = 0;         // their split units (the launch's last)
     int tail_units = 0;     // the last direct units run as tail_pieces pieces each
     int tail_pieces = 0;
+    int group_ctas = 0;     // one-pipeline kernel: CTAs [0, group_ctas) take indices [0,
+    int group_units = 0;    // group_units) first, the others the rest (0: one group)
     long long tail_ws_floats = 0;  // float offset of their partials
     int direct_units = 0;
     int split_units = 0;
@@ -192,15 +195,12 @@ double schedule_end(FinishHeap h) {
 // over more SMs.  Simulates the schedule without pieces and with the last k
 // units in p pieces (k the last wave's units, and that plus half the SMs;
 // p = 2, 3, 4) and keeps the best cut if it ends at least 2% sooner.
-void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
-    const int D = pl.direct_units;
-    if (sms <= 0 || D < sms || D > 8 * sms || pl.split_units > 0 || !(p->flags & CPA_FLAG_TAIL_SPLIT) ||
-        (p->flags & CPA_FLAG_NO_SPLIT))
-        return;
+// Key tiles of every direct unit of a one-tile-per-unit plan, in work-counter
+// order (the order decode_unit uses).
+std::vector<int> direct_unit_tiles(const cpa_batch *b, const cpa_params *p, const Plan &pl) {
     const int G = p->num_heads_q / p->num_heads_kv, hkv = p->num_heads_kv;
-    // key tiles of every direct unit in index order (the order decode_unit uses)
     std::vector<int> tiles;
-    tiles.reserve(D);
+    tiles.reserve(pl.direct_units);
     for (int r = 0; r < b->num_reqs; ++r) {
         const int C = b->h_cached_seq_len[r], N = b->h_num_new_tokens[r];
         const ReqWork w = request_work(C, N, G, hkv, p->head_dim, pl.tile_m, pl.split_len, pl.tiles_per_unit);
@@ -212,6 +212,16 @@ void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
             tiles.push_back(cdiv(C, kTcTileN) + cdiv(last_tok + 1, kTcTileN));
         }
     }
+    return tiles;
+}
+
+void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
+    const int D = pl.direct_units;
+    if (sms <= 0 || D < sms || D > 8 * sms || pl.split_units > 0 || !(p->flags & CPA_FLAG_TAIL_SPLIT) ||
+        (p->flags & CPA_FLAG_NO_SPLIT))
+        return;
+    // key tiles of every direct unit in index order
+    const std::vector<int> tiles = direct_unit_tiles(b, p, pl);
     if ((int)tiles.size() != D) return;
     const int R = D % sms;
     std::vector<int> cuts;
@@ -255,6 +265,94 @@ void plan_tail(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
     if (best < 0 || best > 0.98 * schedule_end(h)) {
         pl.tail_units = 0;
         pl.tail_pieces = 0;
+    }
+}
+
+// Two groups of CTAs for a batch of direct units only (one-pipeline kernel).
+// With U units, heaviest first, on S CTAs (U = q S + R, 0 < R), a single
+// work counter ends in a last wave of R units that the other CTAs wait for.
+// The better packing gives S - R CTAs q of the heaviest units each and R CTAs
+// q + 1 of the lightest: so CTAs [0, S - R) take indices [0, (S - R) q) from
+// the work counter and the others the rest from a second counter, each group
+// in its own greedy order, and a CTA whose group has run out takes the other
+// group's next index.  Simulates both schedules (a unit costs its key tiles
+// plus kGroupSwitchTiles) and keeps the groups if they end at least 2 %
+// sooner: chunks of causal prompts over a cache gain (their units differ by
+// at most 16 tiles of 17-48), a prompt's first chunk (units of 1-16 tiles,
+// already balanced by the single counter) does not, and is not simulated.
+constexpr int kGroupSwitchTiles = 3;
+constexpr int kGroupMaxWaves = 8;
+
+// End of the greedy schedule of units with integer costs (key tiles + the
+// switch) on `sms` CTAs, the first group_ctas of them taking indices
+// [0, group_units) first and the rest the others (group_ctas = 0: one
+// counter).  CTAs of a group are alike, so the simulation keeps, per time
+// step, how many CTAs of each group become free then: no heap.
+int grouped_end(const std::vector<int> &tiles, int sms, int group_ctas, int group_units) {
+    const int U = (int)tiles.size();
+    long long total = 0;
+    int longest = 0;
+    for (int t : tiles) {
+        total += t + kGroupSwitchTiles;
+        longest = std::max(longest, t + kGroupSwitchTiles);
+    }
+    // every CTA is free again by total / sms + longest (a greedy list
+    // schedule ends within one unit of the mean load)
+    const int horizon = (int)(total / sms) + 2 * longest + 2;
+    std::vector<int> free_at[2] = {std::vector<int>(horizon, 0), std::vector<int>(horizon, 0)};
+    free_at[0][0] = group_ctas ? group_ctas : sms;
+    free_at[1][0] = group_ctas ? sms - group_ctas : 0;
+    int next[2] = {0, group_ctas ? group_units : U};
+    const int end[2] = {group_ctas ? group_units : U, U};
+    int last = 0;
+    for (int t = 0; t < horizon; ++t) {
+        for (int g = 0; g < 2; ++g) {
+            for (int c = free_at[g][t]; c > 0; --c) {
+                int u = -1;
+                if (next[g] < end[g])
+                    u = next[g]++;
+                else if (next[1 - g] < end[1 - g])
+                    u = next[1 - g]++;
+                if (u < 0) {
+                    last = t;
+                    continue;
+                }
+                const int f = t + tiles[u] + kGroupSwitchTiles;
+                if (f >= horizon) return INT32_MAX;  // not expected: treated as no gain
+                ++free_at[g][f];
+            }
+        }
+    }
+    return last;
+}
+
+void plan_groups(const cpa_batch *b, const cpa_params *p, int sms, Plan &pl) {
+    const int U = pl.direct_units;
+    if (!pl.tc || pl.tc2 || sms <= 0 || pl.split_units > 0 || pl.tail_units > 0 || pl.head_major || U <= sms ||
+        U > kGroupMaxWaves * sms || U % sms == 0)
+        return;
+    // units more than twice as long as others (a prompt's first chunk) are
+    // balanced by the single counter already: no simulation (host time).  A
+    // request's heaviest unit has all its keys, its lightest those of its
+    // first query tile.
+    const int G = p->num_heads_q / p->num_heads_kv;
+    int lightest = INT32_MAX, heaviest = 0;
+    for (int r = 0; r < b->num_reqs; ++r) {
+        const int C = b->h_cached_seq_len[r], N = b->h_num_new_tokens[r];
+        if (N <= 0) continue;
+        const int first_tok = (std::min(pl.tile_m, N * G) - 1) / G;
+        lightest = std::min(lightest, cdiv(C, kTcTileN) + cdiv(first_tok + 1, kTcTileN));
+        heaviest = std::max(heaviest, cdiv(C, kTcTileN) + cdiv(N, kTcTileN));
+    }
+    if (2 * lightest < heaviest) return;
+    const std::vector<int> tiles = direct_unit_tiles(b, p, pl);
+    if ((int)tiles.size() != U) return;
+    const int q = U / sms, R = U % sms;
+    const int one = grouped_end(tiles, sms, 0, 0);
+    const int two = grouped_end(tiles, sms, sms - R, (sms - R) * q);
+    if (two < INT32_MAX && (double)two < 0.98 * one) {
+        pl.group_ctas = sms - R;
+        pl.group_units = (sms - R) * q;
     }
 }
 
@@ -304,12 +402,14 @@ int choose_tiles_per_unit(const cpa_batch *b, const cpa_params *p, int sms, cons
 }
 
 // Ints at the workspace's counter offset, zeroed before each tensor-core
-// launch: the work counter, kSoftmaxWarpsMax per tail unit, and with the
-// rotary embedding the rotation's claim and done counts and one done count
-// per 128-row tile of the new rows.
+// launch: the work counter, kSoftmaxWarpsMax per tail unit, with the rotary
+// embedding the rotation's claim and done counts and one done count per
+// 128-row tile of the new rows, and with two CTA groups the second group's
+// work counter.
 size_t counter_ints(const cpa_batch *b, const Plan &pl) {
     size_t n = 1 + (size_t)pl.tail_units * kSoftmaxWarpsMax;
     if (pl.rope_fused) n += 2 + (size_t)cdiv(b->total_new_tokens, kTcTileN);
+    if (pl.group_ctas) n += 1;  // the second group's work counter, last
     return n;
 }
 
@@ -393,6 +493,7 @@ Plan make_plan(const cpa_batch *b, const cpa_params *p, int sms) {
                                    .direct_units;
     }
     if (tc) plan_tail(b, p, sms, pl);
+    if (tc) plan_groups(b, p, sms, pl);
     if (pl.tail_units > 0) {
         pl.tail_ws_floats = pl.ws_floats;
         pl.ws_floats += (long long)pl.tail_units * pl.tail_pieces * partial_floats(pl.tile_m, p->head_dim);
@@ -675,6 +776,8 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
     a.num_direct_units = pl.direct_units;
     a.num_split_units = pl.split_units;
     a.tail_units = pl.tail_units;
+    a.group_ctas = pl.group_ctas;
+    a.group_units = pl.group_units;
     a.tail_pieces = pl.tail_pieces;
     a.tail_ws = pl.tail_ws_floats;
     a.q = q;
@@ -729,6 +832,7 @@ cpa_status chunked_prefill_attention(const cpa_batch *batch, const cpa_params *p
         a.sched = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.sched_off);
         a.tail_count = pl.tail_units > 0 ? a.sched + 1 : nullptr;
         a.rope_count = pl.rope_fused ? a.sched + 1 + (size_t)pl.tail_units * kSoftmaxWarpsMax : nullptr;
+        a.sched_b = pl.group_ctas ? a.sched + counter_ints(batch, pl) - 1 : nullptr;
         e = cudaMemsetAsync(a.sched, 0, sizeof(int) * counter_ints(batch, pl), st);
         if (e == cudaSuccess) e = pl.tc2 ? launch_attn_tc2(a, maps, st) : launch_attn_tc(a, maps, st);
     } else {

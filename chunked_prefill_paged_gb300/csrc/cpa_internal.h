@@ -148,6 +148,9 @@ struct AttnArgs {
     float *lse;
     float *ws;          // partials of split units
     int *sched;         // tensor-core kernel: work counter (zeroed before the launch)
+    int group_ctas;     // one-pipeline kernel, two CTA groups (0: one): CTAs [0, group_ctas)
+    int group_units;    // claim indices [0, group_units) from sched, the others the rest
+    int *sched_b;       // from this second counter; each then takes the other group's
     int write_chunks;   // two-pipeline kernel with the fused write: indices [units, units +
                         // write_chunks) of the counter are pieces of the K/V write, taken
                         // by CTAs whose attention work has run out

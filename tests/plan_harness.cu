@@ -55,10 +55,11 @@ int main() {
     printf("{\"split_len\": %d, \"split_len_fine\": %d, \"fine_from\": %d, \"fine_units\": %d, "
            "\"direct_units\": %d, \"split_units\": %d, \"split_reqs\": %d, \"tail_units\": %d, \"tail_pieces\": %d, "
            "\"head_major\": %d, \"interleave_span\": %d, \"ws_bytes\": %zu, \"sched_off\": %zu, "
-           "\"tiles_per_unit\": %d, \"tc2\": %d, \"rope_fused\": %d, \"tile_m\": %d}\n",
+           "\"tiles_per_unit\": %d, \"tc2\": %d, \"rope_fused\": %d, \"tile_m\": %d, \"group_ctas\": %d, "
+           "\"group_units\": %d}\n",
            pl.split_len, pl.split_len_fine, pl.fine_from == INT32_MAX ? -1 : pl.fine_from, pl.fine_units,
            pl.direct_units, pl.split_units, pl.split_reqs, pl.tail_units, pl.tail_pieces, pl.head_major,
            pl.direct_units + pl.split_units - pl.fine_units, pl.ws_bytes, pl.sched_off, pl.tiles_per_unit, pl.tc2 ? 1 : 0,
-           pl.rope_fused ? 1 : 0, pl.tile_m);
+           pl.rope_fused ? 1 : 0, pl.tile_m, pl.group_ctas, pl.group_units);
     return 0;
 }

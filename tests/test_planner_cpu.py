@@ -269,3 +269,27 @@ def test_query_tiles_hold_whole_tokens(harness, hq, hkv, want):
     assert got["tile_m"] == want == G * (128 // G)
     if 128 % G:
         assert got["tc2"] == 0
+
+
+def test_two_cta_groups_for_chunks_over_a_cache(harness):
+    """One-pipeline kernel, direct units only: 512 units on 152 CTAs leave a
+    last wave of 56.  Chunks of 2048 query tokens over a cache (units of
+    17-48 key tiles) pack better as 96 CTAs x 3 of the heaviest units and 56
+    CTAs x 4 of the lightest, each group with its own counter."""
+    for C in (2048, 4096, 6144):
+        p = plan(harness, [(C, 2048)], bs=128)
+        assert (p["tc2"], p["direct_units"]) == (0, 512)
+        assert (p["group_ctas"], p["group_units"]) == (96, 288)
+    # a prompt's first chunk (units of 1-16 tiles: the single counter already
+    # balances them), whole waves, the two-pipeline kernel, split units, the
+    # tail cut: one counter
+    assert plan(harness, [(0, 2048)], bs=128)["group_ctas"] == 0
+    assert plan(harness, [(8192, 1808)], bs=128)["group_ctas"] == 0
+    assert plan(harness, [(4096, 2048)], bs=16)["tc2"] == 1
+    assert plan(harness, [(4096, 2048)], bs=16)["group_ctas"] == 0
+    assert plan(harness, [(4096, 2048), (9000, 1)], bs=128)["group_ctas"] == 0
+    assert plan(harness, [(6144, 2048)], bs=128, flags=FUSE | 0x8)["group_ctas"] == 0
+    # the second counter follows the others in the zeroed counter block
+    one = plan(harness, [(0, 2048)], bs=128)
+    two = plan(harness, [(2048, 2048)], bs=128)
+    assert two["ws_bytes"] - two["sched_off"] == one["ws_bytes"] - one["sched_off"]
