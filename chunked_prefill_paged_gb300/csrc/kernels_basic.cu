@@ -40,8 +40,10 @@ cudaError_t launch_kv_write(const KvWriteArgs &a, int num_sms, cudaStream_t stre
 }
 
 // ------------------------------------------------ rotary / FP8 pre-pass
-// One warp per (active token, group of kHeadsPerWarp heads; query heads first,
-// then key heads; query heads only when rotated queries are wanted).
+// rope_kernel (FP8 pools, fp32 elements): one warp per (active token, group
+// of kHeadsPerWarp heads; query heads first, then key heads; query heads only
+// when rotated queries are wanted).  16-bit rotation alone: rope_rows_kernel
+// below.
 //
 // Rotation: the angle of pair c is reduced to one turn exactly in integer
 // arithmetic: turn_frac[c] holds theta^(-2c/d) / (2 pi) as a 64-bit binary
@@ -237,10 +239,111 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     }
 }
 
+// Rotation only (16-bit elements, no FP8 cache): one warp per active token.
+// Lane l owns the 8-pair chunk c = l mod (d / 16) of a head's half rows --
+// 16 bytes of the first half and the matching 16 bytes of the second -- so it
+// forms its 8 angles once for the token and rotates that chunk of every
+// head, 32 / (d / 16) heads per warp step (query heads first when rotated
+// queries are wanted, then key heads).  kSteps steps have their loads in
+// flight before any of them stores; then the token's value rows go to its
+// pool slot for a fused write.  Same angles and rounding as rope_kernel.
+template <int D, typename T>
+__global__ void __launch_bounds__(256) rope_rows_kernel(RopeArgs a) {
+    static_assert(sizeof(T) == 2, "16-bit elements");
+    constexpr int HALF = D / 2;
+    constexpr int CPH = HALF / 8;        // 8-pair chunks per half row
+    constexpr int HPS = 32 / CPH;        // heads per warp step
+    constexpr int kSteps = 4;            // warp steps with loads in flight at once
+    __shared__ unsigned long long frac_s[HALF];
+    for (int c = threadIdx.x; c < HALF; c += blockDim.x) frac_s[c] = a.turn_frac[c];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const long long t64 = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t64 >= a.total_tokens) return;
+    const int t = (int)t64;
+    const int r = request_of_token(a.cu, a.num_reqs, t);
+    const int pos = __ldg(a.cached + r) + (t - __ldg(a.cu + r));
+    const int c = lane % CPH, hs = lane / CPH;
+    float cs[8], sn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_cos_sin(pos, frac_s[8 * c + e], cs[e], sn[e]);
+    long long slot = -1;
+    if (a.write_pool) slot = slot_of(a.bt, a.max_blocks, a.bs, a.num_blocks, r, pos, a.err);
+    union Chunk {
+        uint4 v;
+        T e[8];
+    };
+    const int head_lo = a.q_rot ? 0 : a.hq;
+    const int heads = a.hq + a.hkv;
+    for (int h0 = head_lo; h0 < heads; h0 += HPS * kSteps) {
+        Chunk lo[kSteps], hi[kSteps];
+#pragma unroll
+        for (int k = 0; k < kSteps; ++k) {
+            const int head = h0 + k * HPS + hs;
+            if (head < heads) {
+                const bool is_q = head < a.hq;
+                const long long row = is_q ? ((long long)t * a.hq + head) * D : ((long long)t * a.hkv + head - a.hq) * D;
+                const T *src = static_cast<const T *>(is_q ? a.q : a.k_new) + row + 8 * c;
+                lo[k].v = __ldg(reinterpret_cast<const uint4 *>(src));
+                hi[k].v = __ldg(reinterpret_cast<const uint4 *>(src + HALF));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kSteps; ++k) {
+            const int head = h0 + k * HPS + hs;
+            if (head >= heads) continue;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float y0, y1;
+                rope_turn(to_float(lo[k].e[e]), to_float(hi[k].e[e]), cs[e], sn[e], y0, y1);
+                lo[k].e[e] = from_float<T>(y0);
+                hi[k].e[e] = from_float<T>(y1);
+            }
+            const bool is_q = head < a.hq;
+            const int hh = is_q ? head : head - a.hq;
+            const long long off = ((long long)t * (is_q ? a.hq : a.hkv) + hh) * D + 8 * c;
+            T *dst = static_cast<T *>(is_q ? a.q_rot : a.k_rot);
+            if (dst) {
+                *reinterpret_cast<uint4 *>(dst + off) = lo[k].v;
+                *reinterpret_cast<uint4 *>(dst + off + HALF) = hi[k].v;
+            }
+            if (!is_q && slot >= 0) {
+                T *kp = static_cast<T *>(a.k_cache) + (slot * a.hkv + hh) * D + 8 * c;
+                *reinterpret_cast<uint4 *>(kp) = lo[k].v;
+                *reinterpret_cast<uint4 *>(kp + HALF) = hi[k].v;
+            }
+        }
+    }
+    if (slot >= 0) {
+        // the token's value rows (all kv heads, contiguous in v_new and in
+        // the slot), unchanged, 16 bytes per lane per step
+        const int chunks = a.hkv * D * 2 / 16;
+        const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v_new) + (long long)t * a.hkv * D);
+        uint4 *vd = reinterpret_cast<uint4 *>(static_cast<T *>(a.v_cache) + slot * a.hkv * D);
+        for (int i0 = lane; i0 < chunks; i0 += 32 * kSteps) {
+            uint4 v[kSteps];
+#pragma unroll
+            for (int k = 0; k < kSteps; ++k)
+                if (i0 + 32 * k < chunks) v[k] = __ldg(vs + i0 + 32 * k);
+#pragma unroll
+            for (int k = 0; k < kSteps; ++k)
+                if (i0 + 32 * k < chunks) vd[i0 + 32 * k] = v[k];
+        }
+    }
+}
+
 cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (a.total_tokens == 0) return cudaSuccess;
     const int warps = 8;
+    if (a.elem_bytes == 2 && a.rotate && !a.kv_fp8 && !a.q8) {
+        const int blocks = (a.total_tokens + warps - 1) / warps;
+        if (a.d == 128)
+            rope_rows_kernel<128, __nv_bfloat16><<<blocks, warps * 32, 0, stream>>>(a);
+        else
+            rope_rows_kernel<64, __nv_bfloat16><<<blocks, warps * 32, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     const int heads = (a.q_rot || a.q8) ? a.hq + a.hkv : a.hkv;
     const long long work = (long long)a.total_tokens * ((heads + kHeadsPerWarp - 1) / kHeadsPerWarp);
     const int blocks = (int)((work + warps - 1) / warps);
