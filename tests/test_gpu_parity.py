@@ -245,3 +245,31 @@ def test_speculative_decode_queries(cpa, variant):
 def test_config_long_context(cpa, variant):
     res = run_and_compare(W.long_context(), rows_per_req=6, steps_to_check=[0, 7, 15], variant=variant)
     assert_within(res, "bf16")
+
+
+# ------------------------------------------------------ two CTA groups (planner)
+@pytest.mark.parametrize("C", [2048, 4096, 6144])
+def test_two_cta_groups_write_every_row(cpa, C):
+    """A chunk of 2048 query tokens over C cached ones (H 32/8, bs 128): 512
+    units on 152 SMs, which the planner runs as two CTA groups, each claiming
+    from its own counter and then from the other's (the planner tests check
+    that choice).  A unit never claimed would leave its rows unwritten: the
+    output and LSE start as NaN and every row must be written; sampled rows
+    match the oracle and the pool's new rows are the oracle's write."""
+    w = small_batch(hq=32, hkv=8, bs=128, seg=1024, reqs=[(C, 2048)], seed=40 + C // 2048)
+    t = w.materialize("cuda")
+    s = w.steps[0]
+    b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
+    p = params_for(w)
+    q, kn, vn = t.step_inputs(s)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((s.total_new_tokens, 32), float("nan"), dtype=torch.float32, device="cuda")
+    n = cpa.workspace_size(b, p)
+    ws = torch.empty((max(n, 16) + 3) // 4, dtype=torch.float32, device="cuda")
+    cpa.chunked_prefill_attention(b, p, q, kn, vn, t.k_cache, t.v_cache, out, lse, ws)
+    torch.cuda.synchronize()
+    assert cpa.last_device_error() == cpa.SUCCESS
+    assert bool(torch.isfinite(out).all()), "output rows left unwritten"
+    assert bool(torch.isfinite(lse).all()), "LSE rows left unwritten"
+    res = run_and_compare(w, rows_per_req=48, seed=C)
+    assert_within(res, "bf16")
