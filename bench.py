@@ -130,6 +130,11 @@ def reduce_max(x: float, world: int) -> float:
     return float(t.item())
 
 
+# nominal dense peaks of one GB300, reported beside the measured fractions
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -370,6 +375,7 @@ def run_ours(args, rank, world, local):
     rec = kernel_traffic_record()
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
+                "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
                 "traffic": rec["bytes_per_launch"] if rec else None,
                 "kernel": "attn_tc_kernel<128, false>",
                 "algorithmic_flops_per_launch": flops_step / len(w.steps)}
@@ -530,6 +536,7 @@ def run_prefill_extra(args, dev, stream, bf16_peak, peak_kind, flush, make, idx)
             "launches_per_step": 1,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": round(achieved / bf16_peak, 4), "peak_kind": f"{peak_kind} bf16 burst",
+                         "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
                          "traffic": None, "kernel": tc_kernel_name(sh, s)},
             "l2": "flushed before every timed call (256 MiB write)"}
 
@@ -593,7 +600,8 @@ def run_mixed(args, dev, stream, hbm_peak, peak_kind, flush, fp8=False):
     return {"workload": w.name + ("_fp8" if fp8 else ""), "metric": "mixed-batch algorithmic GB/s",
             "value": round(gbs, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "bytes_per_step": byts, "tflops": round(flops / (ms / 1e3) / 1e12, 2),
-            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy"}
+            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy",
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
 
 
 def run_case(args, local):
