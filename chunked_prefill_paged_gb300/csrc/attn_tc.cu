@@ -3,7 +3,9 @@
 // (attn_tc_kernel<128, true>).  Persistent: one CTA per SM takes work units
 // (see cpa_internal.h) from a per-launch counter in the workspace, in index
 // order (a request's heaviest units first), so that CTAs that finish early
-// take more units.
+// take more units.  For some prefill batches the planner splits the CTAs into
+// two groups with a counter each (the heaviest units for one, the lightest
+// for the other, claim_unit below), which packs the last wave better.
 //
 // What a unit computes ("Prefill Processing", How Segmentation Works with KV
 // Segments, Kernel Interface, Partial KV Segment Handling; "Prefill
