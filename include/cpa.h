@@ -182,16 +182,19 @@ typedef struct {
  *     The plan depends on the device's SM count: how many of the last
  *     requests take the shorter pieces of the split plan's last wave, and
  *     the tail cut.  With no device present there is neither;
- *   - when rope_theta > 0 (plain pools): the rotated copy of k_new, and on
- *     the CUDA-core kernel of q too;
+ *   - when rope_theta > 0 (plain pools): the rotated copy of k_new, and of
+ *     q too where a pre-pass rotates it (the CUDA-core kernel, and the
+ *     two-pipeline tensor-core kernel that block sizes up to 32 use);
  *   - with the FP8 cache: the two E4M3 planes of q ([2][T, H_q, d] bytes),
  *     its row scales ([T, H_q] x 4 bytes) and the codes of k_new and v_new
  *     ([T, H_kv, d] bytes each);
  *   - when the batch runs on the tensor-core kernel (BF16 with num_heads_q /
- *     num_heads_kv at most 128): that persistent kernel's work counter, one
- *     counter per softmax warp of every tail-cut tile, and with rope_theta >
- *     0 (plain pools) the key rotation's 2 + ceil(T / 128) counters (4 bytes
- *     each, rounded up to 256 bytes).
+ *     num_heads_kv at most 128): that persistent kernel's work counter (a
+ *     second one when the planner splits its CTAs into two groups), one
+ *     counter per softmax warp of every tail-cut tile, and where the
+ *     one-pipeline kernel rotates keys itself (rope_theta > 0, plain pools)
+ *     the key rotation's 2 + ceil(T / 128) counters (4 bytes each, rounded
+ *     up to 256 bytes).
  * 0 for an empty batch and for a CUDA-core batch with no split.  Reads only
  * host mirrors.  Returns 0 also when the arguments are invalid;
  * chunked_prefill_attention then reports the error. */
