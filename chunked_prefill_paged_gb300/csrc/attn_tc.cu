@@ -454,17 +454,25 @@ __device__ __forceinline__ void rope_q_tile(const AttnArgs &a, const Unit &u, ui
     }
 }
 
-// The next work index for this CTA: from its group's counter, then, once
-// that group has run out, from the other's; total_units when both have.
+// Work indices.  A CTA's first unit needs no atomic: CTA b starts with
+// index b of its group (the grid is min(units, SMs), and a group of c CTAs
+// holds at least c units).  Later claims take the group's next index past
+// those, from its counter (zeroed before the launch), then, once the group
+// has run out, the other group's; total_units when both have.
+__device__ __forceinline__ int first_unit(const AttnArgs &a) {
+    if (!a.group_ctas) return (int)blockIdx.x;
+    return (int)blockIdx.x < a.group_ctas ? (int)blockIdx.x : a.group_units + ((int)blockIdx.x - a.group_ctas);
+}
 __device__ __forceinline__ int claim_unit(const AttnArgs &a, int total_units) {
-    if (!a.group_ctas) return atomicAdd(a.sched, 1);
+    if (!a.group_ctas) return (int)gridDim.x + atomicAdd(a.sched, 1);
     const bool first = (int)blockIdx.x < a.group_ctas;
+    const int b_ctas = (int)gridDim.x - a.group_ctas;
     for (int k = 0; k < 2; ++k) {
         if (first == (k == 0)) {
-            const int i = atomicAdd(a.sched, 1);
+            const int i = a.group_ctas + atomicAdd(a.sched, 1);
             if (i < a.group_units) return i;
         } else {
-            const int i = a.group_units + atomicAdd(a.sched_b, 1);
+            const int i = a.group_units + b_ctas + atomicAdd(a.sched_b, 1);
             if (i < total_units) return i;
         }
     }
@@ -577,7 +585,7 @@ __global__ void __launch_bounds__(TcRoles<F8>::kThreads, 1)
         // tile after that, with its Q copy issued then if its stage is free:
         // the next unit's first score MMA need not wait for its queries (nor,
         // with the rotary embedding, for their rotation by the epilogue warps).
-        int taken = (kv_role == 0 && lane == 0) ? claim_unit(a, total_units) : 0;
+        int taken = (kv_role == 0 && lane == 0) ? first_unit(a) : 0;
         int early = -1;        // ring entry published during the previous unit (rotary embedding)
         bool early_q = false;  // and its Q copy issued
         for (int it = 0;; ++it) {  // it: units started by this CTA
