@@ -256,14 +256,27 @@ def test_two_cta_groups_write_every_row(cpa, C):
     that choice).  A unit never claimed would leave its rows unwritten: the
     output and LSE start as NaN and every row must be written; sampled rows
     match the oracle and the pool's new rows are the oracle's write."""
-    w = small_batch(hq=32, hkv=8, bs=128, seg=1024, reqs=[(C, 2048)], seed=40 + C // 2048)
+    _groups_write_every_row(cpa, small_batch(hq=32, hkv=8, bs=128, seg=1024, reqs=[(C, 2048)], seed=40 + C // 2048),
+                            rows_per_req=48, seed=C)
+
+
+def test_two_cta_groups_head_dim_64(cpa):
+    """The same with d 64 and G 1 (H 24/24, bs 128): 384 units, which the
+    planner runs as 72 CTAs taking 2 of the heaviest units and 80 taking 3 of
+    the lightest; a quarter of the rows against the oracle."""
+    _groups_write_every_row(cpa, small_batch(hq=24, hkv=24, d=64, bs=128, seg=1024, reqs=[(2048, 2048)], seed=61),
+                            rows_per_req=512, seed=61)
+
+
+def _groups_write_every_row(cpa, w, rows_per_req, seed):
+    hq = w.shape.num_heads_q
     t = w.materialize("cuda")
     s = w.steps[0]
     b = cpa.Batch(s.cached_seq_len, s.num_new_tokens, w.block_table)
     p = params_for(w)
     q, kn, vn = t.step_inputs(s)
     out = torch.full_like(q, float("nan"))
-    lse = torch.full((s.total_new_tokens, 32), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((s.total_new_tokens, hq), float("nan"), dtype=torch.float32, device="cuda")
     n = cpa.workspace_size(b, p)
     ws = torch.empty((max(n, 16) + 3) // 4, dtype=torch.float32, device="cuda")
     cpa.chunked_prefill_attention(b, p, q, kn, vn, t.k_cache, t.v_cache, out, lse, ws)
@@ -271,5 +284,5 @@ def test_two_cta_groups_write_every_row(cpa, C):
     assert cpa.last_device_error() == cpa.SUCCESS
     assert bool(torch.isfinite(out).all()), "output rows left unwritten"
     assert bool(torch.isfinite(lse).all()), "LSE rows left unwritten"
-    res = run_and_compare(w, rows_per_req=48, seed=C)
+    res = run_and_compare(w, rows_per_req=rows_per_req, seed=seed)
     assert_within(res, "bf16")

@@ -280,6 +280,9 @@ def test_two_cta_groups_for_chunks_over_a_cache(harness):
         p = plan(harness, [(C, 2048)], bs=128)
         assert (p["tc2"], p["direct_units"]) == (0, 512)
         assert (p["group_ctas"], p["group_units"]) == (96, 288)
+    # d 64, G 1: 384 units (q 2, R 80): 72 CTAs x 2 heaviest, 80 x 3 lightest
+    p = plan(harness, [(2048, 2048)], hq=24, hkv=24, d=64, bs=128)
+    assert (p["direct_units"], p["group_ctas"], p["group_units"]) == (384, 72, 144)
     # a prompt's first chunk (units of 1-16 tiles: the single counter already
     # balances them), whole waves, the two-pipeline kernel, split units, the
     # tail cut: one counter
